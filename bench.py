@@ -1,0 +1,478 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused multi-tensor AdamW step on GB300.
+
+Default workload: eight 4096x4096 fp32 tensors with fp32 moments (134,217,728
+parameter elements, 28 bytes of algorithmic traffic per element and step).
+One step is one ``adamw_step`` call (one kernel launch) over every tensor:
+overflow predicate, per-tensor step count and bias-correction scalars, the
+descriptor walk, load/decode, moment and parameter update, encode/store.
+
+Prints ONE JSON line (rank 0):
+  value      parameter-elements per second, whole job (all ranks), inputs resident
+  roofline   achieved algorithmic GB/s of the step kernel vs the measured HBM peak
+  e2e        the same metric through the C ABI with HOST buffers: pinned
+             host->device copy of params, grads and moments, the step, and the
+             device->host copy of params and moments, every step
+  cpu_baseline  the CPU oracle on a bounded sample of the workload (rank 0)
+  clocks     SM clocks sampled by nvidia-smi during the timed region
+
+``--impl reference`` times the CPU oracle instead, on the same metric.
+Under torchrun each rank runs an independent replica ("replicas only": the step
+has no exchange); value = elements of all ranks / the slowest rank's time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+BYTES_PER_ELEM = {  # (param dtype, state kind) -> read + write bytes per element
+    ("f32", "f32"): 28, ("bf16", "f32"): 22, ("f16", "f32"): 22,
+    ("f32", "bf16"): 20, ("bf16", "bf16"): 14, ("f16", "bf16"): 14,
+    ("f32", "int8"): 16.0625, ("bf16", "int8"): 10.0625, ("f16", "int8"): 10.0625,
+}
+FALLBACK_HBM_GBS = 6800.0
+KERNEL_SRC = os.path.join(ROOT, "compact_state_gb300", "csrc", "adamw_kernels.cu")
+
+
+def kernel_hash() -> str:
+    with open(KERNEL_SRC, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+def load_workload(name: str):
+    import workloads
+    return {"few_large": workloads.few_large, "llama3_8b": workloads.llama3_8b,
+            "many_small": workloads.many_small, "lora": workloads.lora,
+            "tiny": workloads.tiny}[name]()
+
+
+def describe(wl, state: str) -> str:
+    shapes = {}
+    for t in wl.tensors:
+        shapes[t.shape] = shapes.get(t.shape, 0) + 1
+    if len(shapes) <= 4:
+        lst = ", ".join(f"{c} x {'x'.join(map(str, s))}" for s, c in shapes.items())
+    else:
+        lst = f"{len(wl.tensors)} tensors"
+    return (f"{wl.name}: {lst}; {wl.param_dtype} params/grads, {state} m/v, "
+            f"{len(wl.groups)} group(s)")
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons (every 100 ms)."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t0 = self.t1 = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self, begin: bool):
+        if begin:
+            self.t0 = time.time()
+        else:
+            self.t1 = time.time()
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((t, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        inside = [r for r in rows if self.t0 is not None and self.t0 - 0.15 <= r[0] <= (self.t1 or 1e30) + 0.15]
+        use = inside or rows
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[k] for r in use for k, v in enumerate(r[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in use),
+                "sm_max_mhz": max(r[2] for r in use), "reasons": reasons,
+                "samples": len(use), "samples_in_timed_region": len(inside)}
+
+
+# ------------------------------------------------------------------ peaks
+def hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def committed_traffic(workload: str, state: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source; else None."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            j = json.load(f)
+        e = j.get(f"{workload}/{state}")
+        if e and e.get("kernel_sha") == kernel_hash():
+            return float(e["dram_bytes_per_launch"])
+    except (OSError, ValueError):
+        pass
+    return None
+
+
+# ------------------------------------------------------------------ oracle
+def _oracle_setup(wl, state, n):
+    import numpy as np
+    from oracle.adamw import new_state
+    big = max(range(len(wl.tensors)), key=lambda i: wl.tensors[i].numel)
+    n = min(wl.tensors[big].numel, n)
+    rng = np.random.default_rng(0)
+    st = [new_state(rng.normal(0, wl.param_std, n), wl.param_dtype, state,
+                    group=wl.tensors[big].group)]
+    groups = [dict(lr=x.lr, beta1=x.beta1, beta2=x.beta2, eps=x.eps,
+                   weight_decay=x.weight_decay) for x in wl.groups]
+    grads = [rng.normal(0, wl.grad_std, n) * wl.grad_prescale for _ in range(2)]
+    return st, groups, grads, n, wl.tensors[big].name
+
+
+def cpu_baseline(wl, state: str, budget_s: float = 12.0, n_max: int = 1 << 21) -> dict:
+    """The oracle, as it is, on a bounded sample: a contiguous slice of the
+    workload's largest tensor, stepped repeatedly for about ``budget_s``."""
+    from oracle.adamw import oracle_step
+    st, groups, grads, n, name = _oracle_setup(wl, state, n_max)
+    steps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle_step(st, groups, [grads[steps % 2]], inv_scale=wl.inv_scale)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return {"value": steps * n / el, "unit": "param-elements/s", "cores": 1,
+            "kind": "oracle",
+            "sample": f"{n} elements of tensor '{name}' ({wl.param_dtype} params, "
+                      f"{state} state), {steps} steps in {el:.1f} s, numpy float64, "
+                      f"one thread"}
+
+
+def reference_arm(wl, state: str, steps: int, warmup: int, n: int = 1 << 18) -> dict:
+    """W untimed + K timed oracle steps, each over a bounded sample of n elements."""
+    from oracle.adamw import oracle_step
+    st, groups, grads, n, name = _oracle_setup(wl, state, n)
+    for k in range(warmup):
+        oracle_step(st, groups, [grads[k % 2]], inv_scale=wl.inv_scale)
+    t0 = time.perf_counter()
+    for k in range(steps):
+        oracle_step(st, groups, [grads[k % 2]], inv_scale=wl.inv_scale)
+    el = time.perf_counter() - t0
+    return {"value": steps * n / el, "unit": "param-elements/s", "cores": 1,
+            "kind": "oracle", "elapsed_s": el,
+            "sample": f"each step: {n} elements of tensor '{name}' ({wl.param_dtype} "
+                      f"params, {state} state), numpy float64, one thread"}
+
+
+# ------------------------------------------------------------------ GPU arm
+def alloc_state(wl, state, dev):
+    import torch
+    import workloads
+    from compact_state_gb300.torch_adapter import AdamWState
+    pdt = workloads.torch_dtype(wl.param_dtype)
+    params = []
+    for i, t in enumerate(wl.tensors):
+        p = torch.empty(t.numel, dtype=pdt, device=dev)
+        p.copy_(workloads.init_param(wl, i, device=dev).reshape(-1))
+        params.append(p)
+    grads = [torch.empty_like(p) for p in params]
+    st = AdamWState(params, grads, state, [t.group for t in wl.tensors])
+    return st
+
+
+def grad_sets(wl, st, n_sets, dev):
+    """Pre-generated grad buffers (seeded, fresh per step up to n_sets)."""
+    import torch
+    import workloads
+    big = max(t.numel for t in wl.tensors)
+    scratch = torch.empty(big, dtype=torch.float32, device=dev)
+    sets = [st.grads]
+    for _ in range(n_sets - 1):
+        sets.append([torch.empty_like(g) for g in st.grads])
+    for k, gs in enumerate(sets):
+        for i, g in enumerate(gs):
+            workloads.fill_grad(wl, i, k + 1, g.view(wl.tensors[i].shape), scratch=scratch)
+    del scratch
+    return sets
+
+
+def run_native(args, wl, rank, world, dev):
+    import torch
+    import compact_state_gb300 as cs
+    from compact_state_gb300 import tensor_desc
+    state = args.state
+    st = alloc_state(wl, state, dev)
+    plan_info = cs.adamw_plan_info(st.plan)
+    # grad buffers: fresh seeded grads per step, cycling through a pool
+    per_set = sum(g.numel() * g.element_size() for g in st.grads)
+    free, _ = torch.cuda.mem_get_info()
+    n_sets = int(max(1, min(args.grad_sets, (free * 0.5) // max(per_set, 1))))
+    sets = grad_sets(wl, st, n_sets, dev)
+    # one plan per grad set (descriptors hold grad pointers)
+    plans = [st.plan]
+    for gs in sets[1:]:
+        descs = [tensor_desc(p, g, m, v, ms, vs, group=t.group)
+                 for p, g, m, v, ms, vs, t in zip(st.params, gs, st.m, st.v, st.m_scale,
+                                                  st.v_scale, wl.tensors)]
+        plans.append(cs.adamw_plan_create(descs, state, 0))
+    groups = cs.groups_array([dict(lr=g.lr, beta1=g.beta1, beta2=g.beta2, eps=g.eps,
+                                   weight_decay=g.weight_decay) for g in wl.groups])
+    ng = len(wl.groups)
+    inv = torch.tensor([wl.inv_scale], dtype=torch.float32, device=dev)
+    fi = torch.zeros(1, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    L = cs.lib()
+    hs = stream.cuda_stream
+
+    def one(k):
+        rc = L.adamw_step(plans[k % len(plans)].handle, groups, ng, None,
+                          st.step.data_ptr(), inv.data_ptr(), fi.data_ptr(), hs)
+        if rc:
+            raise cs.CompactStateError(rc, "adamw_step")
+
+    for k in range(args.warmup):
+        one(k)
+    torch.cuda.synchronize(dev)
+    K = args.steps
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    clk = ClockSampler(dev.index if dev.index is not None else 0)
+    if rank == 0:
+        clk.start()
+        time.sleep(0.3)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clk.mark(True)
+    t0 = time.perf_counter()
+    for k in range(K):
+        starts[k].record(stream)
+        one(args.warmup + k)
+        ends[k].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - t0
+    clk.mark(False)
+    barrier(world)
+    total_ms = starts[0].elapsed_time(ends[-1])
+    per = [starts[k].elapsed_time(ends[k]) for k in range(K)]
+    clocks = clk.stop() if rank == 0 else None
+    max_ms = allreduce_max(total_ms, world, dev)
+    elems = wl.total_numel
+    value = world * elems * K / (max_ms / 1e3)
+    avg_kernel_ms = sum(per) / len(per)
+    bpe = BYTES_PER_ELEM[(wl.param_dtype, state)]
+    alg_bytes = elems * bpe
+    peak, peak_src = hbm_peak()
+    achieved = alg_bytes / (avg_kernel_ms / 1e3) / 1e9
+    traffic = committed_traffic(args.workload, state)
+    result = dict(
+        value=value, ms_per_step=max_ms / K, kernel_ms_avg=avg_kernel_ms,
+        kernel_ms_median=statistics.median(per), wall_s=wall, clocks=clocks,
+        roofline={"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                  "unit": "GB/s", "frac": round(achieved / peak, 4),
+                  "traffic": traffic, "peak_source": f"hbm_gbs of {peak_src}",
+                  "algorithmic_bytes_per_launch": alg_bytes,
+                  "bytes_per_elem": bpe},
+        plan=plan_info, grad_sets=len(plans))
+    for p in plans[1:]:
+        cs.adamw_plan_destroy(p)
+    del sets
+    if not args.no_e2e:
+        result["e2e"] = run_e2e(args, wl, st, groups, ng, dev, world)
+    return result
+
+
+def run_e2e(args, wl, st, groups, ng, dev, world):
+    """Host-resident params, grads and moments: every step copies them in from
+    pinned memory, steps, and copies params and moments back."""
+    import torch
+    import compact_state_gb300 as cs
+    host = []
+    for i in range(len(st.params)):
+        bufs = [st.params[i], st.grads[i], st.m[i], st.v[i]]
+        if st.m_scale[i] is not None:
+            bufs += [st.m_scale[i], st.v_scale[i]]
+        host.append([b.detach().to("cpu").pin_memory() for b in bufs])
+    h2d = sum(b.numel() * b.element_size() for hb in host for b in hb)
+    outs = lambda hb: [hb[0], hb[2], hb[3]] + (hb[4:] if len(hb) > 4 else [])
+    d2h = sum(b.numel() * b.element_size() for hb in host for b in outs(hb))
+    inv = torch.tensor([wl.inv_scale], dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    L = cs.lib()
+
+    def one():
+        for i, hb in enumerate(host):
+            dev_bufs = [st.params[i], st.grads[i], st.m[i], st.v[i]]
+            if st.m_scale[i] is not None:
+                dev_bufs += [st.m_scale[i], st.v_scale[i]]
+            for d, h in zip(dev_bufs, hb):
+                d.copy_(h, non_blocking=True)
+        rc = L.adamw_step(st.plan.handle, groups, ng, None, st.step.data_ptr(),
+                          inv.data_ptr(), None, stream.cuda_stream)
+        if rc:
+            raise cs.CompactStateError(rc, "adamw_step")
+        for i, hb in enumerate(host):
+            dev_bufs = [st.params[i], st.m[i], st.v[i]]
+            if st.m_scale[i] is not None:
+                dev_bufs += [st.m_scale[i], st.v_scale[i]]
+            for d, h in zip(dev_bufs, outs(hb)):
+                h.copy_(d, non_blocking=True)
+
+    K = max(1, min(args.steps, args.e2e_steps))
+    for _ in range(min(2, args.warmup)):
+        one()
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(K):
+        one()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    ms = allreduce_max(e0.elapsed_time(e1), world, dev)
+    return {"value": world * wl.total_numel * K / (ms / 1e3), "unit": "param-elements/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
+            "ms_per_step": ms / K}
+
+
+# ------------------------------------------------------------------ dist
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(x, world, dev):
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device=dev if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def init_dist(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if args.impl == "native" else "gloo"
+        dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default="few_large",
+                    choices=["few_large", "llama3_8b", "many_small", "lora", "tiny"])
+    ap.add_argument("--state", default="f32", choices=["f32", "bf16", "int8"])
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--grad-sets", type=int, default=8)
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0)
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+
+    rank, world, local = init_dist(args)
+    wl = load_workload(args.workload)
+    metric = "AdamW step param-elements/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
+    config = {"workload": describe(wl, args.state), "elements": wl.total_numel,
+              "tensors": len(wl.tensors), "param_dtype": wl.param_dtype,
+              "state": args.state, "groups": len(wl.groups),
+              "l2": "inputs larger than L2 (no flush needed)"
+                    if wl.total_numel * BYTES_PER_ELEM[(wl.param_dtype, args.state)] > 4 * 129e6
+                    else "inputs smaller than L2"}
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        cb = reference_arm(wl, args.state, args.steps, args.warmup)
+        v = cb["value"]
+        line = {"impl": "reference", "metric": metric, "value": v, "unit": "param-elements/s",
+                "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+                "ms_per_step": wl.total_numel / v * 1e3, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic (seeded)", "config": config, "cpu_baseline": cb,
+                "e2e": {"value": v, "unit": "param-elements/s",
+                        "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return 0
+
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the step has no CPU path)")
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    from compact_state_gb300 import build
+    build.build()
+    res = run_native(args, wl, rank, world, dev)
+    if rank != 0:
+        return 0
+    cb = None if args.no_cpu_baseline or world > 1 else cpu_baseline(wl, args.state, args.cpu_budget)
+    line = {"metric": metric, "value": res["value"], "unit": "param-elements/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": res["ms_per_step"], "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded normal params and grads)", "config": config,
+            "roofline": res["roofline"], "clocks": res["clocks"],
+            "e2e": res.get("e2e"), "gpu_launches": args.steps,
+            "kernel_ms_avg": res["kernel_ms_avg"], "kernel_ms_median": res["kernel_ms_median"],
+            "grad_sets": res["grad_sets"], "cpu_baseline": cb}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

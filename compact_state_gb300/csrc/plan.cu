@@ -1,0 +1,421 @@
+// Host side of the C ABI: validation, the work-unit table, the device-resident
+// descriptor tables, and the per-step launch.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "adamw_internal.h"
+
+using cs::TensorDesc;
+using cs::WorkUnit;
+
+struct adamw_plan {
+  int device = 0;
+  int32_t n_tensors = 0;
+  int32_t state_kind = 0;
+  int32_t unit_elems = 0;
+  int32_t max_group = 0;
+  int32_t sm_count = 0;
+  int64_t n_units = 0;
+  int64_t total_numel = 0;
+  int64_t device_bytes = 0;
+  int grid[3] = {0, 0, 0};        // persistent grid per argument class
+  void* dev = nullptr;            // one allocation: descs | units | commit | sched
+  TensorDesc* d_descs = nullptr;
+  WorkUnit* d_units = nullptr;
+  uint32_t* d_commit = nullptr;
+  uint32_t* d_sched = nullptr;
+  std::vector<TensorDesc> h_descs;
+  TensorDesc* h_staging = nullptr;   // pinned, for adamw_plan_set_grads
+  cudaEvent_t staging_done = nullptr;
+  bool staging_pending = false;
+};
+
+namespace {
+
+int elem_bytes(int32_t dtype) {
+  switch (dtype) {
+    case CS_DTYPE_F32: return 4;
+    case CS_DTYPE_BF16: return 2;
+    case CS_DTYPE_F16: return 2;
+    default: return 0;
+  }
+}
+
+int state_elem_bytes(int32_t kind) {
+  switch (kind) {
+    case CS_STATE_F32: return 4;
+    case CS_STATE_BF16: return 2;
+    case CS_STATE_INT8: return 1;
+    default: return 0;
+  }
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Validates one tensor; sets *vec_ok when all buffers allow 4-element vectors.
+int check_tensor(const adamw_tensor_t& t, int32_t state_kind, uint8_t* vec_ok) {
+  if (t.numel < 0 || t.group < 0) return CS_ERR_INVALID_ARGUMENT;
+  const int pb = elem_bytes(t.param_dtype);
+  if (pb == 0) return CS_ERR_UNSUPPORTED;
+  if (t.group >= CS_MAX_GROUPS) return CS_ERR_LIMIT;
+  *vec_ok = 0;
+  if (t.numel == 0) return CS_OK;
+  if (t.numel > (int64_t(1) << 40)) return CS_ERR_LIMIT;
+  const int sb = state_elem_bytes(state_kind);
+  if (!t.param || !t.grad || !t.m || !t.v) return CS_ERR_INVALID_ARGUMENT;
+  if (!aligned(t.param, pb) || !aligned(t.grad, pb) || !aligned(t.m, sb) || !aligned(t.v, sb))
+    return CS_ERR_MISALIGNED;
+  if (state_kind == CS_STATE_INT8) {
+    if (!t.m_scale || !t.v_scale) return CS_ERR_INVALID_ARGUMENT;
+    if (!aligned(t.m_scale, 4) || !aligned(t.v_scale, 4)) return CS_ERR_MISALIGNED;
+  }
+  const bool v = aligned(t.param, 4 * pb) && aligned(t.grad, 4 * pb) &&
+                 aligned(t.m, 4 * sb) && aligned(t.v, 4 * sb);
+  *vec_ok = v ? 1 : 0;
+  return CS_OK;
+}
+
+int check_unit_elems(int32_t unit_elems, int32_t* out) {
+  if (unit_elems == 0) unit_elems = cs::kDefaultUnitElems;
+  if (unit_elems < 0 || unit_elems % cs::kInt8Block != 0 || unit_elems > (1 << 30))
+    return CS_ERR_INVALID_ARGUMENT;
+  *out = unit_elems;
+  return CS_OK;
+}
+
+// Units of every tensor: starts at multiples of unit_elems; the longest first
+// (ties keep tensor order), so a dynamic queue ends on its smallest units. A
+// tensor with no elements gets one empty unit, which only commits its step.
+void build_units(const int64_t* numels, int32_t n, int32_t unit_elems,
+                 std::vector<WorkUnit>* units, std::vector<int32_t>* per_tensor) {
+  units->clear();
+  per_tensor->assign(n, 0);
+  for (int32_t i = 0; i < n; ++i) {
+    const int64_t ne = numels[i];
+    int32_t k = 0;
+    for (int64_t s = 0; s < ne; s += unit_elems, ++k) {
+      WorkUnit w;
+      w.start = s;
+      w.tensor = i;
+      w.len = static_cast<int32_t>(std::min<int64_t>(unit_elems, ne - s));
+      units->push_back(w);
+    }
+    if (ne == 0) {            // an empty tensor still counts its steps
+      units->push_back(WorkUnit{0, i, 0});
+      k = 1;
+    }
+    (*per_tensor)[i] = k;
+  }
+  std::stable_sort(units->begin(), units->end(),
+                   [](const WorkUnit& a, const WorkUnit& b) { return a.len > b.len; });
+}
+
+bool finite_f(float x) { return std::isfinite(x); }
+
+int check_group(const adamw_group_t& g) {
+  if (!finite_f(g.lr) || !finite_f(g.eps) || !finite_f(g.weight_decay)) return CS_ERR_HYPERPARAM;
+  if (!(g.beta1 >= 0.0f && g.beta1 < 1.0f)) return CS_ERR_HYPERPARAM;
+  if (!(g.beta2 >= 0.0f && g.beta2 < 1.0f)) return CS_ERR_HYPERPARAM;
+  if (g.eps < 0.0f) return CS_ERR_HYPERPARAM;
+  return CS_OK;
+}
+
+template <int G, int W>
+int launch_class(adamw_plan* p, cs::ArgClass cls, const adamw_group_t* groups,
+                 int32_t n_groups, const uint32_t* present, int32_t* step,
+                 const float* inv_scale, const float* found_inf, cudaStream_t stream) {
+  cs::StepArgs<G, W> a;
+  std::memset(&a, 0, sizeof(a));
+  a.descs = p->d_descs;
+  a.units = p->d_units;
+  a.step = step;
+  a.inv_scale = inv_scale;
+  a.found_inf = found_inf;
+  a.sched = p->d_sched;
+  a.commit = p->d_commit;
+  a.n_units = static_cast<int32_t>(p->n_units);
+  std::memcpy(a.groups, groups, sizeof(adamw_group_t) * n_groups);
+  if (present) {
+    a.all_present = 0;
+    std::memcpy(a.present, present, sizeof(uint32_t) * ((p->n_tensors + 31) / 32));
+  } else {
+    a.all_present = 1;
+  }
+  const cudaError_t e = cs::launch_step(p->state_kind, cls, &a, p->grid[cls], stream);
+  return e == cudaSuccess ? CS_OK : CS_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* adamw_strerror(int status) {
+  switch (status) {
+    case CS_OK: return "success";
+    case CS_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case CS_ERR_UNSUPPORTED: return "unsupported dtype or state kind";
+    case CS_ERR_MISALIGNED: return "pointer not aligned to its element size";
+    case CS_ERR_LIMIT: return "size limit exceeded (tensors, groups, elements or capacity)";
+    case CS_ERR_CUDA: return "CUDA runtime error";
+    case CS_ERR_OUT_OF_MEMORY: return "out of memory";
+    case CS_ERR_HYPERPARAM: return "invalid hyper-parameter (beta outside [0,1), negative eps or non-finite value)";
+    case CS_ERR_WRONG_DEVICE: return "current CUDA device is not the plan's device";
+    default: return "unknown status";
+  }
+}
+
+int adamw_state_bytes(const int64_t* numels, int32_t n_tensors, int32_t state_kind,
+                      int64_t* out_bytes) {
+  if (!out_bytes || n_tensors < 0 || (n_tensors > 0 && !numels)) return CS_ERR_INVALID_ARGUMENT;
+  const int sb = state_elem_bytes(state_kind);
+  if (sb == 0) return CS_ERR_UNSUPPORTED;
+  int64_t total = 0;
+  for (int32_t i = 0; i < n_tensors; ++i) {
+    const int64_t n = numels[i];
+    if (n < 0) return CS_ERR_INVALID_ARGUMENT;
+    total += 2 * sb * n + 4;   // two moments + a 4-byte step counter
+    if (state_kind == CS_STATE_INT8) total += 2 * 4 * ((n + cs::kInt8Block - 1) / cs::kInt8Block);
+  }
+  *out_bytes = total;
+  return CS_OK;
+}
+
+int adamw_build_units(const int64_t* numels, int32_t n_tensors, int32_t unit_elems,
+                      int32_t* tensor_out, int64_t* start_out, int32_t* len_out,
+                      int64_t cap, int64_t* n_units_out) {
+  if (!n_units_out || n_tensors < 0 || (n_tensors > 0 && !numels) || cap < 0)
+    return CS_ERR_INVALID_ARGUMENT;
+  int32_t ue = 0;
+  int rc = check_unit_elems(unit_elems, &ue);
+  if (rc) return rc;
+  for (int32_t i = 0; i < n_tensors; ++i)
+    if (numels[i] < 0) return CS_ERR_INVALID_ARGUMENT;
+  try {
+    std::vector<WorkUnit> units;
+    std::vector<int32_t> per;
+    build_units(numels, n_tensors, ue, &units, &per);
+    *n_units_out = static_cast<int64_t>(units.size());
+    if (static_cast<int64_t>(units.size()) > cap) return cap == 0 ? CS_OK : CS_ERR_LIMIT;
+    if (!tensor_out || !start_out || !len_out) return CS_ERR_INVALID_ARGUMENT;
+    for (size_t k = 0; k < units.size(); ++k) {
+      tensor_out[k] = units[k].tensor;
+      start_out[k] = units[k].start;
+      len_out[k] = units[k].len;
+    }
+  } catch (const std::bad_alloc&) {
+    return CS_ERR_OUT_OF_MEMORY;
+  }
+  return CS_OK;
+}
+
+int adamw_plan_create(const adamw_tensor_t* tensors, int32_t n_tensors, int32_t state_kind,
+                      int32_t unit_elems, adamw_plan_t** out_plan) {
+  if (!out_plan) return CS_ERR_INVALID_ARGUMENT;
+  *out_plan = nullptr;
+  if (!tensors || n_tensors <= 0) return CS_ERR_INVALID_ARGUMENT;
+  if (n_tensors > CS_MAX_TENSORS) return CS_ERR_LIMIT;
+  if (state_elem_bytes(state_kind) == 0) return CS_ERR_UNSUPPORTED;
+  int32_t ue = 0;
+  int rc = check_unit_elems(unit_elems, &ue);
+  if (rc) return rc;
+
+  adamw_plan* p = nullptr;
+  try {
+    p = new adamw_plan();
+    p->n_tensors = n_tensors;
+    p->state_kind = state_kind;
+    p->unit_elems = ue;
+    p->h_descs.resize(n_tensors);
+    std::vector<int64_t> numels(n_tensors);
+    for (int32_t i = 0; i < n_tensors; ++i) {
+      const adamw_tensor_t& t = tensors[i];
+      uint8_t vec = 0;
+      rc = check_tensor(t, state_kind, &vec);
+      if (rc) { delete p; return rc; }
+      TensorDesc& d = p->h_descs[i];
+      std::memset(&d, 0, sizeof(d));
+      d.param = t.param;
+      d.grad = t.grad;
+      d.m = t.m;
+      d.v = t.v;
+      d.m_scale = state_kind == CS_STATE_INT8 ? t.m_scale : nullptr;
+      d.v_scale = state_kind == CS_STATE_INT8 ? t.v_scale : nullptr;
+      d.numel = t.numel;
+      d.group = static_cast<int16_t>(t.group);
+      d.param_dtype = static_cast<uint8_t>(t.param_dtype);
+      d.vec_ok = vec;
+      numels[i] = t.numel;
+      p->total_numel += t.numel;
+      p->max_group = std::max(p->max_group, t.group);
+    }
+    std::vector<WorkUnit> units;
+    std::vector<int32_t> per;
+    build_units(numels.data(), n_tensors, ue, &units, &per);
+    if (units.size() >= (size_t(1) << 31) - (size_t(1) << 20)) { delete p; return CS_ERR_LIMIT; }
+    for (int32_t i = 0; i < n_tensors; ++i) p->h_descs[i].n_units = per[i];
+    p->n_units = static_cast<int64_t>(units.size());
+
+    if (cudaGetDevice(&p->device) != cudaSuccess) { delete p; return CS_ERR_CUDA; }
+    if (cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
+      delete p; return CS_ERR_CUDA;
+    }
+    for (int c = 0; c < 3; ++c) {
+      int per_sm = 0;
+      if (cs::step_kernel_occupancy(state_kind, static_cast<cs::ArgClass>(c), &per_sm) != cudaSuccess ||
+          per_sm <= 0) {
+        delete p; return CS_ERR_CUDA;
+      }
+      const int64_t want = static_cast<int64_t>(per_sm) * p->sm_count;
+      // never more CTAs than units (at least one)
+      p->grid[c] = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, p->n_units)));
+    }
+
+    const size_t b_desc = sizeof(TensorDesc) * n_tensors;
+    const size_t b_units = sizeof(WorkUnit) * std::max<size_t>(units.size(), 1);
+    const size_t b_commit = ((sizeof(uint32_t) * n_tensors + 255) / 256) * 256;
+    const size_t b_sched = 256;
+    const size_t total = b_desc + b_units + b_commit + b_sched;
+    if (cudaMalloc(&p->dev, total) != cudaSuccess) {
+      cudaGetLastError();
+      delete p;
+      return CS_ERR_OUT_OF_MEMORY;
+    }
+    p->device_bytes = static_cast<int64_t>(total);
+    char* base = static_cast<char*>(p->dev);
+    p->d_descs = reinterpret_cast<TensorDesc*>(base);
+    p->d_units = reinterpret_cast<WorkUnit*>(base + b_desc);
+    p->d_commit = reinterpret_cast<uint32_t*>(base + b_desc + b_units);
+    p->d_sched = reinterpret_cast<uint32_t*>(base + b_desc + b_units + b_commit);
+    bool ok = cudaMemcpy(p->d_descs, p->h_descs.data(), b_desc, cudaMemcpyHostToDevice) == cudaSuccess;
+    if (ok && !units.empty())
+      ok = cudaMemcpy(p->d_units, units.data(), sizeof(WorkUnit) * units.size(),
+                      cudaMemcpyHostToDevice) == cudaSuccess;
+    ok = ok && cudaMemset(p->d_commit, 0, b_commit + b_sched) == cudaSuccess;
+    ok = ok && cudaDeviceSynchronize() == cudaSuccess;
+    if (!ok) {
+      cudaFree(p->dev);
+      delete p;
+      return CS_ERR_CUDA;
+    }
+  } catch (const std::bad_alloc&) {
+    if (p) {
+      if (p->dev) cudaFree(p->dev);
+      delete p;
+    }
+    return CS_ERR_OUT_OF_MEMORY;
+  }
+  *out_plan = p;
+  return CS_OK;
+}
+
+int adamw_step(adamw_plan_t* p, const adamw_group_t* groups, int32_t n_groups,
+               const uint32_t* grad_present, int32_t* step, const float* inv_scale,
+               const float* found_inf, struct CUstream_st* stream) {
+  if (!p || !groups || !step) return CS_ERR_INVALID_ARGUMENT;
+  if (n_groups <= 0) return CS_ERR_INVALID_ARGUMENT;
+  if (n_groups > CS_MAX_GROUPS) return CS_ERR_LIMIT;
+  if (p->max_group >= n_groups) return CS_ERR_INVALID_ARGUMENT;
+  for (int32_t g = 0; g < n_groups; ++g) {
+    const int rc = check_group(groups[g]);
+    if (rc) return rc;
+  }
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CS_ERR_CUDA;
+  if (dev != p->device) return CS_ERR_WRONG_DEVICE;
+
+  cs::ArgClass cls;
+  const int32_t need_tensors = grad_present ? p->n_tensors : 0;
+  if (n_groups <= cs::kSmallGroups && need_tensors <= cs::kSmallWords * 32) cls = cs::kClassSmall;
+  else if (need_tensors <= cs::kMidWords * 32) cls = cs::kClassMid;
+  else cls = cs::kClassLarge;
+
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  switch (cls) {
+    case cs::kClassSmall:
+      return launch_class<cs::kSmallGroups, cs::kSmallWords>(p, cls, groups, n_groups, grad_present,
+                                                             step, inv_scale, found_inf, s);
+    case cs::kClassMid:
+      return launch_class<cs::kMidGroups, cs::kMidWords>(p, cls, groups, n_groups, grad_present,
+                                                         step, inv_scale, found_inf, s);
+    default:
+      return launch_class<cs::kLargeGroups, cs::kLargeWords>(p, cls, groups, n_groups, grad_present,
+                                                             step, inv_scale, found_inf, s);
+  }
+}
+
+int adamw_plan_set_grads(adamw_plan_t* p, const void* const* grads, struct CUstream_st* stream) {
+  if (!p || !grads) return CS_ERR_INVALID_ARGUMENT;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CS_ERR_CUDA;
+  if (dev != p->device) return CS_ERR_WRONG_DEVICE;
+  // validate first: nothing changes on error
+  for (int32_t i = 0; i < p->n_tensors; ++i) {
+    const TensorDesc& d = p->h_descs[i];
+    if (d.numel == 0) continue;
+    const int pb = elem_bytes(d.param_dtype);
+    if (!grads[i]) return CS_ERR_INVALID_ARGUMENT;
+    if (!aligned(grads[i], pb)) return CS_ERR_MISALIGNED;
+  }
+  const size_t bytes = sizeof(TensorDesc) * p->n_tensors;
+  if (!p->h_staging) {
+    if (cudaMallocHost(reinterpret_cast<void**>(&p->h_staging), bytes) != cudaSuccess) {
+      cudaGetLastError();
+      p->h_staging = nullptr;
+      return CS_ERR_OUT_OF_MEMORY;
+    }
+    if (cudaEventCreateWithFlags(&p->staging_done, cudaEventDisableTiming) != cudaSuccess)
+      return CS_ERR_CUDA;
+  }
+  if (p->staging_pending && cudaEventSynchronize(p->staging_done) != cudaSuccess) return CS_ERR_CUDA;
+  for (int32_t i = 0; i < p->n_tensors; ++i) {
+    TensorDesc& d = p->h_descs[i];
+    if (d.numel == 0) continue;
+    const int pb = elem_bytes(d.param_dtype);
+    const int sb = state_elem_bytes(p->state_kind);
+    d.grad = grads[i];
+    d.vec_ok = (aligned(d.param, 4 * pb) && aligned(d.grad, 4 * pb) && aligned(d.m, 4 * sb) &&
+                aligned(d.v, 4 * sb)) ? 1 : 0;
+  }
+  std::memcpy(p->h_staging, p->h_descs.data(), bytes);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(p->d_descs, p->h_staging, bytes, cudaMemcpyHostToDevice, s) != cudaSuccess)
+    return CS_ERR_CUDA;
+  if (cudaEventRecord(p->staging_done, s) != cudaSuccess) return CS_ERR_CUDA;
+  p->staging_pending = true;
+  return CS_OK;
+}
+
+int adamw_plan_info(const adamw_plan_t* p, adamw_plan_info_t* out) {
+  if (!p || !out) return CS_ERR_INVALID_ARGUMENT;
+  out->n_units = p->n_units;
+  out->total_numel = p->total_numel;
+  out->device_bytes = p->device_bytes;
+  out->n_tensors = p->n_tensors;
+  out->state_kind = p->state_kind;
+  out->unit_elems = p->unit_elems;
+  out->grid_blocks = p->grid[cs::kClassSmall];
+  out->block_threads = cs::kThreads;
+  out->device = p->device;
+  return CS_OK;
+}
+
+int adamw_plan_destroy(adamw_plan_t* p) {
+  if (!p) return CS_OK;
+  int rc = CS_OK;
+  int prev = -1;
+  cudaGetDevice(&prev);
+  if (prev != p->device) cudaSetDevice(p->device);
+  if (cudaDeviceSynchronize() != cudaSuccess) rc = CS_ERR_CUDA;
+  if (p->dev && cudaFree(p->dev) != cudaSuccess) rc = CS_ERR_CUDA;
+  if (p->staging_done) cudaEventDestroy(p->staging_done);
+  if (p->h_staging) cudaFreeHost(p->h_staging);
+  if (prev >= 0 && prev != p->device) cudaSetDevice(prev);
+  delete p;
+  return rc;
+}
+
+}  // extern "C"

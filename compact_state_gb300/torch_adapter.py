@@ -1,0 +1,73 @@
+"""Torch-side holder of one parameter set's optimizer state.
+
+Allocates zeroed moment buffers (and int8 block scales), the per-tensor int32
+step counters, and the plan, using torch only for device memory; the step
+itself is ``adamw_step`` in the CUDA library.
+"""
+from __future__ import annotations
+
+from typing import List, Optional, Sequence
+
+import torch
+
+from ._binding import (CS_INT8_BLOCK, Plan, adamw_plan_create, adamw_plan_set_grads,
+                       adamw_step, pack_present, tensor_desc)
+
+STATE_TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "int8": torch.int8}
+
+
+class AdamWState:
+    """Moments, scales and step counts for ``params`` (flat per tensor).
+
+    params, grads: same-length lists of CUDA tensors (grads same dtype/numel).
+    group_of: per-tensor group index (default 0).
+    """
+
+    def __init__(self, params: Sequence[torch.Tensor], grads: Sequence[torch.Tensor],
+                 state_kind: str = "f32", group_of: Optional[Sequence[int]] = None,
+                 unit_elems: int = 0):
+        if len(params) != len(grads):
+            raise ValueError("params and grads differ in length")
+        self.params = list(params)
+        self.grads = list(grads)
+        self.state_kind = state_kind
+        n = len(self.params)
+        self.group_of = list(group_of) if group_of is not None else [0] * n
+        sdt = STATE_TORCH_DTYPE[state_kind]
+        dev = self.params[0].device if n else torch.device("cuda")
+        self.m: List[torch.Tensor] = []
+        self.v: List[torch.Tensor] = []
+        self.m_scale: List[Optional[torch.Tensor]] = []
+        self.v_scale: List[Optional[torch.Tensor]] = []
+        descs = []
+        for p, g, grp in zip(self.params, self.grads, self.group_of):
+            if p.numel() != g.numel() or p.dtype != g.dtype:
+                raise ValueError("grad must match its param in numel and dtype")
+            ne = p.numel()
+            m = torch.zeros(ne, dtype=sdt, device=dev)
+            v = torch.zeros(ne, dtype=sdt, device=dev)
+            if state_kind == "int8":
+                nb = -(-ne // CS_INT8_BLOCK)
+                ms = torch.zeros(max(nb, 1), dtype=torch.float32, device=dev)
+                vs = torch.zeros(max(nb, 1), dtype=torch.float32, device=dev)
+            else:
+                ms = vs = None
+            self.m.append(m)
+            self.v.append(v)
+            self.m_scale.append(ms)
+            self.v_scale.append(vs)
+            descs.append(tensor_desc(p, g, m, v, ms, vs, group=grp))
+        self.step = torch.zeros(max(n, 1), dtype=torch.int32, device=dev)
+        self.plan: Plan = adamw_plan_create(descs, state_kind, unit_elems)
+
+    def run(self, groups, present=None, inv_scale=None, found_inf=None, stream=None):
+        """One optimizer step (asynchronous on ``stream``)."""
+        bits = None if present is None else pack_present(present, len(self.params))
+        adamw_step(self.plan, groups, bits, self.step, inv_scale, found_inf, stream)
+
+    def set_grads(self, grads: Sequence[torch.Tensor], stream=None) -> None:
+        self.grads = list(grads)
+        adamw_plan_set_grads(self.plan, self.grads, stream)
+
+    def state_tensors(self, i: int):
+        return self.m[i], self.v[i], self.m_scale[i], self.v_scale[i]

@@ -1,0 +1,227 @@
+/*
+ * compact_state.h -- C ABI of the fused multi-tensor AdamW step for GB300.
+ *
+ * One call, adamw_step(), runs one AdamW optimizer step over a whole list of
+ * parameter tensors in a single persistent kernel launch. Moment state is kept
+ * as fp32, compact bf16, or block-wise signed 8-bit codes.
+ *
+ * What the step computes is the AdamW update of "Fused Optimizers and State
+ * Precision" (xuujii.github.io ai-infra-kb M041), section 02, for every element
+ * of every tensor that has a gradient, with t the tensor's own step count:
+ *
+ *     t = t + 1
+ *     m = beta1*m + (1-beta1)*g
+ *     v = beta2*v + (1-beta2)*g*g
+ *     theta = theta*(1-lr*wd) - lr * (m/(1-beta1^t)) / (sqrt(v/(1-beta2^t)) + eps)
+ *
+ * with g = stored_grad * inv_scale (the grad-scaler unscale of the Apex
+ * FusedAdam capturable path, Apex fused-optimizers guide section 4.3). The bias
+ * corrections are per-tensor scalars; m_hat and v_hat are never stored
+ * (section 04). The theta update uses the freshly updated moments before they
+ * are re-encoded (section 05: decode -> update -> re-encode).
+ *
+ * Contract (sections 02, 03, 06 of the same page):
+ *   - every parameter group has its own lr, betas, eps and weight decay;
+ *   - a tensor without a gradient this step (grad=None) is not touched at all:
+ *     no decay, no moment update, no step advance; a zero gradient IS a full
+ *     update;
+ *   - when *found_inf != 0 the whole step is a no-op: params, moments, scales
+ *     and step counts are left bit-identical.
+ *
+ * Conventions for every function:
+ *   - Return value 0 (CS_OK) on success, a negative CS_ERR_* code otherwise;
+ *     adamw_strerror() names it. No function aborts or throws across the ABI.
+ *   - "device" pointers are CUDA global-memory addresses on the device that was
+ *     current when the plan was created; "host" pointers are ordinary memory.
+ *   - The caller owns every buffer it passes (params, grads, moments, scales,
+ *     step counters, inv_scale, found_inf); they must outlive the plan. The
+ *     plan owns only its own device tables, freed by adamw_plan_destroy().
+ *   - Only adamw_plan_create / adamw_plan_destroy allocate or free device
+ *     memory. adamw_step() allocates nothing, never synchronises the host and
+ *     is asynchronous on the given stream.
+ *   - A plan must not be stepped concurrently on two streams.
+ */
+#ifndef COMPACT_STATE_H
+#define COMPACT_STATE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st;              /* cudaStream_t is `struct CUstream_st *` */
+
+/* ---- status codes ------------------------------------------------------ */
+#define CS_OK                    0
+#define CS_ERR_INVALID_ARGUMENT (-1)  /* null/negative/out-of-range argument   */
+#define CS_ERR_UNSUPPORTED      (-2)  /* unknown dtype or state kind          */
+#define CS_ERR_MISALIGNED       (-3)  /* pointer not aligned to its element   */
+#define CS_ERR_LIMIT            (-4)  /* too many tensors / groups / elements */
+#define CS_ERR_CUDA             (-5)  /* a CUDA runtime call failed           */
+#define CS_ERR_OUT_OF_MEMORY    (-6)  /* host or device allocation failed     */
+#define CS_ERR_HYPERPARAM       (-7)  /* beta outside [0,1), non-finite lr... */
+#define CS_ERR_WRONG_DEVICE     (-8)  /* current device is not the plan's     */
+
+/* ---- element types ----------------------------------------------------- */
+#define CS_DTYPE_F32   0         /* params / grads                          */
+#define CS_DTYPE_BF16  1
+#define CS_DTYPE_F16   2
+
+#define CS_STATE_F32   0         /* two fp32 moments per element            */
+#define CS_STATE_BF16  1         /* two bf16 moments per element (RNE)      */
+#define CS_STATE_INT8  2         /* two int8 codes per element + two fp32
+                                    scales per 256-element block            */
+
+#define CS_INT8_BLOCK        256     /* elements per int8 scale block       */
+#define CS_MAX_GROUPS        64      /* parameter groups per step           */
+#define CS_MAX_TENSORS       245760  /* tensors per plan                    */
+
+/* ---- one parameter group's hyper-parameters (host memory, per step) ---- */
+typedef struct adamw_group_t {
+    float lr;            /* learning rate, finite                            */
+    float beta1;         /* in [0, 1)                                        */
+    float beta2;         /* in [0, 1)                                        */
+    float eps;           /* finite, >= 0, added outside the square root      */
+    float weight_decay;  /* decoupled decay: theta *= 1 - lr*weight_decay    */
+} adamw_group_t;
+
+/* ---- one parameter tensor (host memory, read by adamw_plan_create) ----- */
+typedef struct adamw_tensor_t {
+    void       *param;   /* device, numel elements of param_dtype, in place  */
+    const void *grad;    /* device, numel elements of param_dtype (stored,
+                            i.e. still multiplied by the loss scale)         */
+    void       *m;       /* device, first moment: numel fp32 / bf16 values,
+                            or numel int8 codes for CS_STATE_INT8            */
+    void       *v;       /* device, second moment, same layout as m          */
+    float      *m_scale; /* device, CS_STATE_INT8 only: ceil(numel/256) fp32
+                            scales of m, one per 256-element block of the
+                            tensor's flat order (else ignored, may be NULL)  */
+    float      *v_scale; /* device, CS_STATE_INT8 only: scales of v          */
+    int64_t     numel;   /* elements, >= 0 (0: no buffer is touched, but the
+                            step count still advances when it has a grad)    */
+    int32_t     param_dtype;  /* CS_DTYPE_*; grad has the same dtype         */
+    int32_t     group;        /* index into the per-step group table         */
+} adamw_tensor_t;
+
+/* Moments start at zero: the caller zero-fills m and v (and, for int8, the
+ * codes and the scales) before the first step. Pointers need only be aligned
+ * to their element size; when every buffer of a tensor is also aligned to
+ * four elements the kernel uses vector loads for it.                        */
+
+typedef struct adamw_plan adamw_plan_t;
+
+typedef struct adamw_plan_info_t {
+    int64_t n_units;        /* work units in the device queue               */
+    int64_t total_numel;    /* sum of numel over the plan's tensors          */
+    int64_t device_bytes;   /* device memory owned by the plan               */
+    int32_t n_tensors;
+    int32_t state_kind;
+    int32_t unit_elems;     /* elements per work unit                        */
+    int32_t grid_blocks;    /* CTAs of the persistent launch                 */
+    int32_t block_threads;  /* threads per CTA                               */
+    int32_t device;         /* CUDA device ordinal of the plan               */
+} adamw_plan_info_t;
+
+/*
+ * adamw_plan_create -- validate a tensor list and upload its descriptor and
+ * work-unit tables to the current device, once per parameter set.
+ *   tensors     host array [n_tensors], read only during the call.
+ *   n_tensors   1 .. CS_MAX_TENSORS.
+ *   state_kind  CS_STATE_*; one kind for all tensors of the plan.
+ *   unit_elems  elements per work unit; 0 picks the default (32768). Must be
+ *               a positive multiple of 256 otherwise.
+ *   out_plan    host out-parameter; set to NULL on failure.
+ * Allocates device memory (descriptors 64 B/tensor, units 16 B/unit,
+ * a 4 B/tensor commit counter and an 8 B scheduler word). Synchronous.
+ * Errors: CS_ERR_INVALID_ARGUMENT, CS_ERR_UNSUPPORTED, CS_ERR_MISALIGNED,
+ * CS_ERR_LIMIT, CS_ERR_OUT_OF_MEMORY, CS_ERR_CUDA.
+ */
+int adamw_plan_create(const adamw_tensor_t *tensors, int32_t n_tensors,
+                      int32_t state_kind, int32_t unit_elems,
+                      adamw_plan_t **out_plan);
+
+/*
+ * adamw_step -- one fused AdamW step over every tensor of the plan, enqueued
+ * on `stream` as one kernel launch.
+ *   groups        host array [n_groups] (copied into the launch; may be freed
+ *                 on return). Every tensor's group must be < n_groups.
+ *   n_groups      1 .. CS_MAX_GROUPS.
+ *   grad_present  host bitmask [ceil(n_tensors/32)] (copied into the launch):
+ *                 bit (i % 32) of word (i / 32) set means tensor i has a
+ *                 gradient this step. NULL means every tensor has one.
+ *   step          device int32 [n_tensors]: per-tensor step counts. The kernel
+ *                 uses t = step[i] + 1 and stores t back only for tensors it
+ *                 updated, and only when the step is not skipped.
+ *   inv_scale     device fp32 scalar multiplied into every gradient; NULL = 1.
+ *   found_inf     device fp32 scalar; nonzero (or NaN) skips the whole step.
+ *                 NULL = 0.
+ *   stream        CUDA stream (NULL = legacy default stream).
+ * Allocates nothing, does not synchronise, can be captured in a CUDA graph
+ * (the group table and bitmask are captured by value).
+ * Errors (nothing is enqueued): CS_ERR_INVALID_ARGUMENT, CS_ERR_HYPERPARAM,
+ * CS_ERR_LIMIT, CS_ERR_WRONG_DEVICE; CS_ERR_CUDA if the launch fails.
+ */
+int adamw_step(adamw_plan_t *plan, const adamw_group_t *groups, int32_t n_groups,
+               const uint32_t *grad_present, int32_t *step,
+               const float *inv_scale, const float *found_inf,
+               struct CUstream_st *stream);
+
+/*
+ * adamw_plan_set_grads -- replace the gradient pointers of every tensor (for
+ * frameworks that reallocate gradients between steps).
+ *   grads   host array [n_tensors] of device pointers (NULL allowed only for
+ *           tensors with numel 0); alignment rules as at creation.
+ *   stream  the stream later steps use; the table update is ordered on it.
+ * Copies through a plan-owned pinned staging buffer; it waits on the host only
+ * if the previous call's copy has not yet left that buffer.
+ * Errors: CS_ERR_INVALID_ARGUMENT, CS_ERR_MISALIGNED, CS_ERR_CUDA.
+ */
+int adamw_plan_set_grads(adamw_plan_t *plan, const void *const *grads,
+                         struct CUstream_st *stream);
+
+/* adamw_plan_info -- fill *out (host) with the plan's sizes and launch shape. */
+int adamw_plan_info(const adamw_plan_t *plan, adamw_plan_info_t *out);
+
+/* adamw_plan_destroy -- synchronise the device and free the plan's tables.
+ * NULL is accepted. The caller's buffers are untouched.                      */
+int adamw_plan_destroy(adamw_plan_t *plan);
+
+/*
+ * adamw_state_bytes -- bytes of optimizer state for a tensor list, host only:
+ * moments (8 / 4 / 2 bytes per element for fp32 / bf16 / int8), plus for int8
+ * two fp32 scales per 256-element block of each tensor, plus a 4-byte step
+ * counter per tensor. Section 05's payload ledger; the ApexW Unsloth benchmark
+ * page's 185.501 / 92.751 / 47.101 MB for its LoRA set follow from it.
+ *   numels  host array [n_tensors]; out: host int64.
+ * Errors: CS_ERR_INVALID_ARGUMENT, CS_ERR_UNSUPPORTED.
+ */
+int adamw_state_bytes(const int64_t *numels, int32_t n_tensors, int32_t state_kind,
+                      int64_t *out_bytes);
+
+/*
+ * adamw_build_units -- the plan's work-unit table, computed on the host only
+ * (no CUDA call), for inspection and tests. Units are (tensor, start, len)
+ * with start a multiple of unit_elems, len <= unit_elems, covering each
+ * tensor exactly once, ordered longest first; a tensor with numel 0 has one
+ * unit of len 0.
+ *   numels      host [n_tensors];  unit_elems as for adamw_plan_create.
+ *   tensor_out, start_out, len_out  host arrays of capacity `cap` (may be NULL
+ *               when cap is 0, to query the count).
+ *   n_units_out host int64: the number of units (always written).
+ * Errors: CS_ERR_INVALID_ARGUMENT, CS_ERR_LIMIT (cap too small: nothing but
+ * *n_units_out written).
+ */
+int adamw_build_units(const int64_t *numels, int32_t n_tensors, int32_t unit_elems,
+                      int32_t *tensor_out, int64_t *start_out, int32_t *len_out,
+                      int64_t cap, int64_t *n_units_out);
+
+/* adamw_strerror -- static string naming a status code (never NULL). */
+const char *adamw_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* COMPACT_STATE_H */

@@ -1,0 +1,168 @@
+"""Host-side checks of the C ABI that need no GPU.
+
+* the library builds, loads, and exports every function include/compact_state.h
+  declares; the binding's constants equal the header's;
+* adamw_state_bytes reproduces the oracle's ledger and the pages' figures;
+* the work-unit table covers every tensor exactly once;
+* invalid plans and steps are rejected with status codes before any CUDA call.
+"""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import workloads
+from oracle import state_bytes as ostate
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "compact_state.h")
+
+
+@pytest.fixture(scope="module")
+def cs():
+    from compact_state_gb300 import build
+    build.build()
+    import compact_state_gb300 as m
+    m.lib()
+    return m
+
+
+def _header_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\s*\*?\s*(adamw_\w+)\s*\(", src, re.M)))
+
+
+def _header_defines():
+    out = {}
+    for name, val in re.findall(r"#define\s+(CS_\w+)\s+\(?(-?\d+)\)?", open(HEADER).read()):
+        out[name] = int(val)
+    return out
+
+
+def test_exports_every_declared_symbol(cs):
+    declared = _header_functions()
+    assert len(declared) == 8, declared
+    assert sorted(cs.EXPORTS) == declared
+    L = cs.lib()
+    for name in declared:
+        assert hasattr(L, name), name
+    out = os.popen(f"nm -D {cs.lib()._name}").read()
+    for name in declared:
+        assert re.search(rf"\bT {name}\b", out), name
+
+
+def test_constants_match_header(cs):
+    import compact_state_gb300._binding as b
+    defs = _header_defines()
+    assert defs, "no #defines parsed"
+    for name, val in defs.items():
+        assert getattr(b, name) == val, name
+
+
+def test_strerror_names_every_code(cs):
+    for code in range(0, -9, -1):
+        s = cs.adamw_strerror(code)
+        assert s and s != "unknown status"
+    assert cs.adamw_strerror(-99) == "unknown status"
+
+
+@pytest.mark.parametrize("kind", ["f32", "bf16", "int8"])
+def test_state_bytes_equals_oracle_ledger(cs, kind):
+    rng = np.random.default_rng(0)
+    numels = [0, 1, 255, 256, 257] + list(rng.integers(1, 10 ** 6, 50))
+    assert cs.adamw_state_bytes(numels, kind) == ostate.state_bytes(numels, kind)
+    lora = workloads.lora()
+    mib = round(cs.adamw_state_bytes(lora.numels, kind) / 2 ** 20, 3)
+    assert mib == {"f32": 185.501, "bf16": 92.751, "int8": 47.101}[kind]
+
+
+def test_state_bytes_rejects_bad_input(cs):
+    with pytest.raises(cs.CompactStateError):
+        cs.adamw_state_bytes([5, -1], "f32")
+    with pytest.raises(KeyError):
+        cs.adamw_state_bytes([5], "f8")
+    assert cs.lib().adamw_state_bytes(None, 0, 7, ctypes.byref(ctypes.c_int64())) == -2
+
+
+@pytest.mark.parametrize("unit", [256, 1024, 32768])
+def test_work_units_tile_every_tensor_once(cs, unit):
+    rng = np.random.default_rng(unit)
+    numels = [0, 1, 3, unit - 1, unit, unit + 1, 3 * unit + 17] + list(
+        rng.integers(1, 20 * unit, 40))
+    t, s, ln = cs.adamw_build_units(numels, unit)
+    t, s, ln = np.array(t), np.array(s), np.array(ln)
+    assert ln.sum() == sum(numels)
+    assert np.all(ln <= unit) and np.all(s % unit == 0)
+    assert np.all((ln > 0) | (np.array(numels)[t] == 0))
+    assert np.all(np.diff(ln) <= 0), "units must be ordered longest first"
+    for i, n in enumerate(numels):
+        sel = t == i
+        order = np.argsort(s[sel])
+        ss, ll = s[sel][order], ln[sel][order]
+        if n == 0:
+            assert sel.sum() == 1 and ln[sel][0] == 0
+            continue
+        assert ss[0] == 0 and np.all(ss[1:] == ss[:-1] + ll[:-1]) and ss[-1] + ll[-1] == n
+
+
+def test_work_units_reject_bad_unit_size(cs):
+    for bad in (-256, 100, 257):
+        with pytest.raises(cs.CompactStateError):
+            cs.adamw_build_units([10], bad)
+
+
+def _desc(cs, **kw):
+    base = dict(param=0x10000, grad=0x20000, m=0x30000, v=0x40000, m_scale=0x50000,
+                v_scale=0x60000, numel=100, param_dtype=0, group=0)
+    base.update(kw)
+    return cs.adamw_tensor_t(**base)
+
+
+@pytest.mark.parametrize("kw,state,code", [
+    (dict(param_dtype=5), "f32", -2),
+    (dict(numel=-1), "f32", -1),
+    (dict(group=-1), "f32", -1),
+    (dict(group=64), "f32", -4),
+    (dict(param=0), "f32", -1),
+    (dict(grad=0x20002), "f32", -3),          # fp32 grad not 4-byte aligned
+    (dict(param=0x10001, param_dtype=1), "bf16", -3),
+    (dict(m=0x30002), "f32", -3),
+    (dict(m_scale=0), "int8", -1),
+    (dict(v_scale=0x60002), "int8", -3),
+])
+def test_plan_create_rejects_invalid_tensors(cs, kw, state, code):
+    arr = (cs.adamw_tensor_t * 2)(_desc(cs), _desc(cs, **kw))
+    out = ctypes.c_void_p(123)
+    rc = cs.lib().adamw_plan_create(arr, 2, cs.STATE_CODES[state], 0, ctypes.byref(out))
+    assert rc == code and out.value is None
+
+
+def test_plan_create_rejects_bad_arguments(cs):
+    L = cs.lib()
+    arr = (cs.adamw_tensor_t * 1)(_desc(cs))
+    out = ctypes.c_void_p()
+    assert L.adamw_plan_create(None, 1, 0, 0, ctypes.byref(out)) == -1
+    assert L.adamw_plan_create(arr, 0, 0, 0, ctypes.byref(out)) == -1
+    assert L.adamw_plan_create(arr, 1, 3, 0, ctypes.byref(out)) == -2
+    assert L.adamw_plan_create(arr, 1, 0, 100, ctypes.byref(out)) == -1
+    assert L.adamw_plan_create(arr, 1, 0, 0, None) == -1
+    assert L.adamw_plan_create(arr, 245761, 0, 0, ctypes.byref(out)) == -4
+
+
+def test_step_rejects_null_plan(cs):
+    g = (cs.adamw_group_t * 1)(cs.adamw_group_t(1e-3, 0.9, 0.999, 1e-8, 0.0))
+    assert cs.lib().adamw_step(None, g, 1, None, 0x1000, None, None, None) == -1
+    assert cs.lib().adamw_plan_info(None, None) == -1
+    assert cs.lib().adamw_plan_destroy(None) == 0
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_valid_plan_without_gpu_reports_cuda_error(cs):
+    arr = (cs.adamw_tensor_t * 1)(_desc(cs))
+    out = ctypes.c_void_p()
+    assert cs.lib().adamw_plan_create(arr, 1, 0, 0, ctypes.byref(out)) == -5
+    assert out.value is None
