@@ -64,7 +64,8 @@ class CompactStateError(RuntimeError):
 
 _LIB = None
 EXPORTS = ("adamw_plan_create", "adamw_step", "adamw_plan_set_grads", "adamw_plan_info",
-           "adamw_plan_destroy", "adamw_state_bytes", "adamw_build_units", "adamw_strerror")
+           "adamw_plan_destroy", "adamw_state_bytes", "adamw_build_units", "adamw_strerror",
+           "adamw_plan_error", "adamw_plan_set_debug")
 
 
 def lib() -> ctypes.CDLL:
@@ -89,6 +90,8 @@ def lib() -> ctypes.CDLL:
     L.adamw_build_units.argtypes = [ctypes.POINTER(i64), i32, i32, ctypes.POINTER(i32),
                                     ctypes.POINTER(i64), ctypes.POINTER(i32), i64,
                                     ctypes.POINTER(i64)]
+    L.adamw_plan_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
+    L.adamw_plan_set_debug.argtypes = [vp, ctypes.c_uint64, ctypes.c_uint32]
     L.adamw_strerror.argtypes = [ctypes.c_int]
     L.adamw_strerror.restype = ctypes.c_char_p
     for name in EXPORTS:
@@ -223,6 +226,19 @@ def adamw_plan_info(plan: Plan) -> dict:
     info = adamw_plan_info_t()
     _check(lib().adamw_plan_info(plan.handle, ctypes.byref(info)), "adamw_plan_info")
     return {k: getattr(info, k) for k, _ in adamw_plan_info_t._fields_}
+
+
+def adamw_plan_error(plan: Plan) -> int:
+    """Read and clear the plan's device error word (synchronises the device)."""
+    out = ctypes.c_uint32()
+    _check(lib().adamw_plan_error(plan.handle, ctypes.byref(out)), "adamw_plan_error")
+    return out.value
+
+
+def adamw_plan_set_debug(plan: Plan, wait_ns: int = 0, flags: int = 0) -> None:
+    """Test hook: bound on every in-kernel wait and debug flags."""
+    _check(lib().adamw_plan_set_debug(plan.handle, int(wait_ns), int(flags)),
+           "adamw_plan_set_debug")
 
 
 def adamw_plan_destroy(plan: Plan) -> None:

@@ -9,10 +9,51 @@
 
 namespace cs {
 
-constexpr int kThreads = 256;              // threads per CTA of the step kernel
-constexpr int kWarps = kThreads / 32;
-constexpr int kDefaultUnitElems = 32768;   // elements per work unit
+#ifndef CS_CONSUMER_WARPS
+#define CS_CONSUMER_WARPS 16
+#endif
+
+constexpr int kConsumerWarps = CS_CONSUMER_WARPS;      // compute warps per CTA
+constexpr int kConsumerThreads = 32 * kConsumerWarps;
+constexpr int kThreads = 32 + kConsumerThreads;        // + one producer warp
+constexpr int kDefaultUnitElems = 32768;               // elements per work unit
 constexpr int kInt8Block = CS_INT8_BLOCK;
+constexpr int kStageBudget = 200 * 1024;               // dynamic shared memory for stages
+constexpr uint64_t kDefaultWaitNs = 2000000000ull;     // 2 s bound on every wait
+
+// Elements per pipeline stage: one 4-element group per compute thread for
+// fp32/bf16 moments, one 256-element block per compute warp for int8.
+constexpr int tile_elems(int state_kind) {
+  return state_kind == CS_STATE_INT8 ? kConsumerWarps * kInt8Block : kConsumerThreads * 4;
+}
+// Bytes of one pipeline stage for a state kind (params sized for fp32, the
+// widest param type, since the param type varies per tensor).
+constexpr int stage_bytes(int state_kind) {
+  return state_kind == CS_STATE_F32    ? tile_elems(state_kind) * 16
+         : state_kind == CS_STATE_BF16 ? tile_elems(state_kind) * 12
+                                       : tile_elems(state_kind) * 10 +
+                                             2 * (tile_elems(state_kind) / kInt8Block) * 4;
+}
+constexpr int stages_for(int state_kind) {
+  return kStageBudget / ((stage_bytes(state_kind) + 127) / 128 * 128) > 8
+             ? 8
+             : kStageBudget / ((stage_bytes(state_kind) + 127) / 128 * 128);
+}
+static_assert(tile_elems(CS_STATE_INT8) % 1024 == 0 && tile_elems(CS_STATE_F32) % 1024 == 0,
+              "tiles hold whole int8 blocks in 16-byte scale groups");
+static_assert(kDefaultUnitElems % tile_elems(CS_STATE_INT8) == 0 &&
+              kDefaultUnitElems % tile_elems(CS_STATE_F32) == 0, "units hold whole tiles");
+
+// Error bits the kernel sets in the plan's error word (never traps).
+enum : uint32_t {
+  kErrConsumerWait = 1u,   // a compute warp gave up waiting for a tile
+  kErrProducerWait = 2u,   // the producer gave up waiting for a tile's compute
+  kErrDrainWait = 4u,      // the producer gave up waiting for its own loads
+};
+// Debug flags (test hook; 0 in normal use).
+enum : uint32_t {
+  kDebugSkipFirstTile = 1u,   // the first tile of the queue's first unit is never signalled
+};
 
 // One tensor, as the kernel sees it. 64 bytes, one per tensor.
 struct alignas(16) TensorDesc {
@@ -25,10 +66,15 @@ struct alignas(16) TensorDesc {
   int64_t numel;
   int16_t group;
   uint8_t param_dtype;   // CS_DTYPE_*
-  uint8_t vec_ok;        // every buffer aligned for 4-element vector access
+  uint8_t flags;         // kVec | kBulk
   int32_t n_units;       // work units of this tensor (commit counter target)
 };
 static_assert(sizeof(TensorDesc) == 64, "descriptor must stay 64 bytes");
+enum : uint8_t {
+  kVec = 1,    // every buffer aligned to four elements: vector loads
+  kBulk = 2,   // every buffer 16-byte aligned: bulk (TMA) copies
+  kBulkScale = 4,  // int8 scale arrays 16-byte aligned
+};
 
 // One work unit: `len` elements of tensor `tensor` starting at `start`.
 struct alignas(16) WorkUnit {
@@ -50,8 +96,12 @@ struct StepArgs {
   const float* found_inf;    // may be null (0)
   uint32_t* sched;           // [2]: next unit ticket, CTAs finished
   uint32_t* commit;          // [n_tensors]: units of each tensor started
+  uint32_t* err;             // error bits (kErr*)
+  uint64_t wait_ns;          // bound on every wait
+  uint32_t debug;            // kDebug* flags
   int32_t n_units;
   int32_t all_present;       // 1: ignore `present`
+  int32_t pad_;
   adamw_group_t groups[MAXG];
   uint32_t present[MAXW];
 };
@@ -68,7 +118,8 @@ enum ArgClass { kClassSmall = 0, kClassMid = 1, kClassLarge = 2 };
 // Launch one step. Defined in adamw_kernels.cu.
 cudaError_t launch_step(int state_kind, ArgClass cls, const void* args,
                         int grid, cudaStream_t stream);
-// Max resident CTAs per SM of the kernel for (state_kind, cls).
+// Max resident CTAs per SM of the kernel for (state_kind, cls); also sets the
+// kernel's dynamic shared memory limit.
 cudaError_t step_kernel_occupancy(int state_kind, ArgClass cls, int* blocks_per_sm);
 
 }  // namespace cs

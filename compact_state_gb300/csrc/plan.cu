@@ -27,7 +27,9 @@ struct adamw_plan {
   TensorDesc* d_descs = nullptr;
   WorkUnit* d_units = nullptr;
   uint32_t* d_commit = nullptr;
-  uint32_t* d_sched = nullptr;
+  uint32_t* d_sched = nullptr;     // [0] next unit, [1] CTAs done, [2] error bits
+  uint64_t wait_ns = cs::kDefaultWaitNs;
+  uint32_t debug = 0;
   std::vector<TensorDesc> h_descs;
   TensorDesc* h_staging = nullptr;   // pinned, for adamw_plan_set_grads
   cudaEvent_t staging_done = nullptr;
@@ -56,7 +58,17 @@ int state_elem_bytes(int32_t kind) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-// Validates one tensor; sets *vec_ok when all buffers allow 4-element vectors.
+uint8_t access_flags(const void* param, const void* grad, const void* m, const void* v,
+                     const float* ms, const float* vs, int pb, int sb, int32_t state_kind) {
+  uint8_t f = 0;
+  if (aligned(param, 4 * pb) && aligned(grad, 4 * pb) && aligned(m, 4 * sb) && aligned(v, 4 * sb))
+    f |= cs::kVec;
+  if (aligned(param, 16) && aligned(grad, 16) && aligned(m, 16) && aligned(v, 16)) f |= cs::kBulk;
+  if (state_kind == CS_STATE_INT8 && aligned(ms, 16) && aligned(vs, 16)) f |= cs::kBulkScale;
+  return f;
+}
+
+// Validates one tensor; sets *flags to its access flags (vector, bulk).
 int check_tensor(const adamw_tensor_t& t, int32_t state_kind, uint8_t* vec_ok) {
   if (t.numel < 0 || t.group < 0) return CS_ERR_INVALID_ARGUMENT;
   const int pb = elem_bytes(t.param_dtype);
@@ -73,9 +85,7 @@ int check_tensor(const adamw_tensor_t& t, int32_t state_kind, uint8_t* vec_ok) {
     if (!t.m_scale || !t.v_scale) return CS_ERR_INVALID_ARGUMENT;
     if (!aligned(t.m_scale, 4) || !aligned(t.v_scale, 4)) return CS_ERR_MISALIGNED;
   }
-  const bool v = aligned(t.param, 4 * pb) && aligned(t.grad, 4 * pb) &&
-                 aligned(t.m, 4 * sb) && aligned(t.v, 4 * sb);
-  *vec_ok = v ? 1 : 0;
+  *vec_ok = access_flags(t.param, t.grad, t.m, t.v, t.m_scale, t.v_scale, pb, sb, state_kind);
   return CS_OK;
 }
 
@@ -137,6 +147,9 @@ int launch_class(adamw_plan* p, cs::ArgClass cls, const adamw_group_t* groups,
   a.found_inf = found_inf;
   a.sched = p->d_sched;
   a.commit = p->d_commit;
+  a.err = p->d_sched + 2;
+  a.wait_ns = p->wait_ns;
+  a.debug = p->debug;
   a.n_units = static_cast<int32_t>(p->n_units);
   std::memcpy(a.groups, groups, sizeof(adamw_group_t) * n_groups);
   if (present) {
@@ -247,7 +260,7 @@ int adamw_plan_create(const adamw_tensor_t* tensors, int32_t n_tensors, int32_t 
       d.numel = t.numel;
       d.group = static_cast<int16_t>(t.group);
       d.param_dtype = static_cast<uint8_t>(t.param_dtype);
-      d.vec_ok = vec;
+      d.flags = vec;
       numels[i] = t.numel;
       p->total_numel += t.numel;
       p->max_group = std::max(p->max_group, t.group);
@@ -377,8 +390,8 @@ int adamw_plan_set_grads(adamw_plan_t* p, const void* const* grads, struct CUstr
     const int pb = elem_bytes(d.param_dtype);
     const int sb = state_elem_bytes(p->state_kind);
     d.grad = grads[i];
-    d.vec_ok = (aligned(d.param, 4 * pb) && aligned(d.grad, 4 * pb) && aligned(d.m, 4 * sb) &&
-                aligned(d.v, 4 * sb)) ? 1 : 0;
+    d.flags = access_flags(d.param, d.grad, d.m, d.v, d.m_scale, d.v_scale, pb, sb,
+                           p->state_kind);
   }
   std::memcpy(p->h_staging, p->h_descs.data(), bytes);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -386,6 +399,32 @@ int adamw_plan_set_grads(adamw_plan_t* p, const void* const* grads, struct CUstr
     return CS_ERR_CUDA;
   if (cudaEventRecord(p->staging_done, s) != cudaSuccess) return CS_ERR_CUDA;
   p->staging_pending = true;
+  return CS_OK;
+}
+
+int adamw_plan_error(adamw_plan_t* p, uint32_t* out_flags) {
+  if (!p || !out_flags) return CS_ERR_INVALID_ARGUMENT;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CS_ERR_CUDA;
+  if (dev != p->device) return CS_ERR_WRONG_DEVICE;
+  uint32_t v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) return CS_ERR_CUDA;
+  if (cudaMemcpy(&v, p->d_sched + 2, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return CS_ERR_CUDA;
+  const uint32_t zero = 0;
+  if (cudaMemcpy(p->d_sched + 2, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return CS_ERR_CUDA;
+  *out_flags = v;
+  return CS_OK;
+}
+
+int adamw_plan_set_debug(adamw_plan_t* p, uint64_t wait_ns, uint32_t flags) {
+  if (!p) return CS_ERR_INVALID_ARGUMENT;
+  if (wait_ns == 0) wait_ns = cs::kDefaultWaitNs;
+  if (wait_ns > 60ull * 1000000000ull || (flags & ~uint32_t(cs::kDebugSkipFirstTile)))
+    return CS_ERR_INVALID_ARGUMENT;
+  p->wait_ns = wait_ns;
+  p->debug = flags;
   return CS_OK;
 }
 

@@ -134,7 +134,8 @@ typedef struct adamw_plan_info_t {
  *               a positive multiple of 256 otherwise.
  *   out_plan    host out-parameter; set to NULL on failure.
  * Allocates device memory (descriptors 64 B/tensor, units 16 B/unit,
- * a 4 B/tensor commit counter and an 8 B scheduler word). Synchronous.
+ * a 4 B/tensor commit counter, two scheduler words and an error word).
+ * Synchronous.
  * Errors: CS_ERR_INVALID_ARGUMENT, CS_ERR_UNSUPPORTED, CS_ERR_MISALIGNED,
  * CS_ERR_LIMIT, CS_ERR_OUT_OF_MEMORY, CS_ERR_CUDA.
  */
@@ -180,6 +181,28 @@ int adamw_step(adamw_plan_t *plan, const adamw_group_t *groups, int32_t n_groups
  */
 int adamw_plan_set_grads(adamw_plan_t *plan, const void *const *grads,
                          struct CUstream_st *stream);
+
+/*
+ * adamw_plan_error -- read and clear the plan's device error word (host out).
+ * Every wait inside the step kernel is bounded (2 s by default). A wait that
+ * runs out sets a bit here and that CTA winds down without touching its
+ * remaining tiles; nothing traps and the CUDA context stays usable. Bits:
+ * 1 a compute warp gave up waiting for a tile, 2 the producer gave up waiting
+ * for a tile's compute, 4 the producer gave up waiting for its own loads.
+ * 0 means every step since the last call ran to completion. Synchronises the
+ * device. Errors: CS_ERR_INVALID_ARGUMENT, CS_ERR_WRONG_DEVICE, CS_ERR_CUDA.
+ */
+int adamw_plan_error(adamw_plan_t *plan, uint32_t *out_flags);
+
+/*
+ * adamw_plan_set_debug -- test hook for later steps of this plan: the bound
+ * on every wait in nanoseconds (0 restores the 2 s default; at most 60 s) and
+ * debug flags. Flag 1 leaves the first tile of the queue's first unit
+ * unsignalled, so that the bounded waits of the CTA holding it run out and
+ * report through adamw_plan_error. Normal use never calls it.
+ * Errors: CS_ERR_INVALID_ARGUMENT (unknown flag or bound above 60 s).
+ */
+int adamw_plan_set_debug(adamw_plan_t *plan, uint64_t wait_ns, uint32_t flags);
 
 /* adamw_plan_info -- fill *out (host) with the plan's sizes and launch shape. */
 int adamw_plan_info(const adamw_plan_t *plan, adamw_plan_info_t *out);

@@ -45,7 +45,7 @@ def _header_defines():
 
 def test_exports_every_declared_symbol(cs):
     declared = _header_functions()
-    assert len(declared) == 8, declared
+    assert len(declared) == 10, declared
     assert sorted(cs.EXPORTS) == declared
     L = cs.lib()
     for name in declared:
@@ -157,6 +157,8 @@ def test_step_rejects_null_plan(cs):
     g = (cs.adamw_group_t * 1)(cs.adamw_group_t(1e-3, 0.9, 0.999, 1e-8, 0.0))
     assert cs.lib().adamw_step(None, g, 1, None, 0x1000, None, None, None) == -1
     assert cs.lib().adamw_plan_info(None, None) == -1
+    assert cs.lib().adamw_plan_error(None, None) == -1
+    assert cs.lib().adamw_plan_set_debug(None, 0, 0) == -1
     assert cs.lib().adamw_plan_destroy(None) == 0
 
 

