@@ -41,12 +41,18 @@ BYTES_PER_ELEM = {  # (param dtype, state kind) -> read + write bytes per elemen
     ("f32", "int8"): 16.0625, ("bf16", "int8"): 10.0625, ("f16", "int8"): 10.0625,
 }
 FALLBACK_HBM_GBS = 6800.0
-KERNEL_SRC = os.path.join(ROOT, "compact_state_gb300", "csrc", "adamw_kernels.cu")
+KERNEL_SRCS = [os.path.join(ROOT, "compact_state_gb300", "csrc", f)
+               for f in ("adamw_kernels.cu", "adamw_internal.h")]
 
 
 def kernel_hash() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of the step kernel's sources (a committed traffic figure is only
+    reported while it matches)."""
+    h = hashlib.sha256()
+    for path in KERNEL_SRCS:
+        with open(path, "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 def load_workload(name: str):
