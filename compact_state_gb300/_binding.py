@@ -29,6 +29,9 @@ CS_STATE_INT8 = 2
 CS_INT8_BLOCK = 256
 CS_MAX_GROUPS = 64
 CS_MAX_TENSORS = 245760
+CS_NOALLOC_MAX_TENSORS = 4096
+CS_NOALLOC_MAX_UNITS = 65536
+CS_NOALLOC_UNIT = 32768
 
 DTYPE_CODES = {"f32": CS_DTYPE_F32, "bf16": CS_DTYPE_BF16, "f16": CS_DTYPE_F16}
 STATE_CODES = {"f32": CS_STATE_F32, "bf16": CS_STATE_BF16, "int8": CS_STATE_INT8}
@@ -65,7 +68,7 @@ class CompactStateError(RuntimeError):
 _LIB = None
 EXPORTS = ("adamw_plan_create", "adamw_step", "adamw_plan_set_grads", "adamw_plan_info",
            "adamw_plan_destroy", "adamw_state_bytes", "adamw_build_units", "adamw_strerror",
-           "adamw_plan_error", "adamw_plan_set_debug")
+           "adamw_plan_error", "adamw_plan_set_debug", "adamw_step_noalloc")
 
 
 def lib() -> ctypes.CDLL:
@@ -92,6 +95,9 @@ def lib() -> ctypes.CDLL:
                                     ctypes.POINTER(i64)]
     L.adamw_plan_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     L.adamw_plan_set_debug.argtypes = [vp, ctypes.c_uint64, ctypes.c_uint32]
+    L.adamw_step_noalloc.argtypes = [ctypes.POINTER(adamw_tensor_t), i32, i32,
+                                     ctypes.POINTER(adamw_group_t), i32,
+                                     ctypes.POINTER(ctypes.c_uint32), vp, vp, vp, vp]
     L.adamw_strerror.argtypes = [ctypes.c_int]
     L.adamw_strerror.restype = ctypes.c_char_p
     for name in EXPORTS:
@@ -214,6 +220,22 @@ def adamw_step(plan: Plan, groups, grad_present=None, step=None, inv_scale=None,
     rc = lib().adamw_step(plan.handle, ga, n_groups, grad_present, _ptr(step),
                           _ptr(inv_scale), _ptr(found_inf), _stream(stream))
     _check(rc, "adamw_step")
+
+
+def adamw_step_noalloc(tensors: Sequence[adamw_tensor_t], state_kind, groups,
+                       grad_present=None, step=None, inv_scale=None, found_inf=None,
+                       stream=None) -> None:
+    """One step without a plan and without any device allocation (see the
+    header: shared fixed-size scratch, first call per device sets it up)."""
+    sk = STATE_CODES[state_kind] if isinstance(state_kind, str) else int(state_kind)
+    arr = (adamw_tensor_t * max(len(tensors), 1))(*tensors)
+    ga = groups if isinstance(groups, ctypes.Array) else groups_array(groups)
+    if grad_present is not None and not isinstance(grad_present, ctypes.Array):
+        grad_present = pack_present(grad_present, len(tensors))
+    rc = lib().adamw_step_noalloc(arr, len(tensors), sk, ga, len(groups), grad_present,
+                                  _ptr(step), _ptr(inv_scale), _ptr(found_inf),
+                                  _stream(stream))
+    _check(rc, "adamw_step_noalloc")
 
 
 def adamw_plan_set_grads(plan: Plan, grads: Sequence, stream=None) -> None:

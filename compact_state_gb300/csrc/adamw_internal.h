@@ -16,7 +16,7 @@ namespace cs {
 constexpr int kConsumerWarps = CS_CONSUMER_WARPS;      // compute warps per CTA
 constexpr int kConsumerThreads = 32 * kConsumerWarps;
 constexpr int kThreads = 32 + kConsumerThreads;        // + one producer warp
-constexpr int kDefaultUnitElems = 32768;               // elements per work unit
+constexpr int kDefaultUnitElems = CS_NOALLOC_UNIT;     // elements per work unit
 constexpr int kInt8Block = CS_INT8_BLOCK;
 constexpr int kStageBudget = 200 * 1024;               // dynamic shared memory for stages
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;     // 2 s bound on every wait
@@ -114,6 +114,14 @@ static_assert(sizeof(StepArgs<kLargeGroups, kLargeWords>) <= 32764,
               "kernel parameter space");
 
 enum ArgClass { kClassSmall = 0, kClassMid = 1, kClassLarge = 2 };
+
+// Host-side validation shared by the entry points (defined in plan.cu).
+namespace host {
+int elem_bytes(int32_t dtype);
+int state_elem_bytes(int32_t kind);
+int check_tensor(const adamw_tensor_t& t, int32_t state_kind, uint8_t* flags);
+int check_group(const adamw_group_t& g);
+}  // namespace host
 
 // Launch one step. Defined in adamw_kernels.cu.
 cudaError_t launch_step(int state_kind, ArgClass cls, const void* args,

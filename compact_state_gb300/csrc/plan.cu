@@ -36,7 +36,8 @@ struct adamw_plan {
   bool staging_pending = false;
 };
 
-namespace {
+namespace cs {
+namespace host {
 
 int elem_bytes(int32_t dtype) {
   switch (dtype) {
@@ -124,7 +125,19 @@ void build_units(const int64_t* numels, int32_t n, int32_t unit_elems,
                    [](const WorkUnit& a, const WorkUnit& b) { return a.len > b.len; });
 }
 
+}  // namespace host
+}  // namespace cs
+
+using namespace cs::host;
+
+namespace {
+
 bool finite_f(float x) { return std::isfinite(x); }
+
+}  // namespace
+
+namespace cs {
+namespace host {
 
 int check_group(const adamw_group_t& g) {
   if (!finite_f(g.lr) || !finite_f(g.eps) || !finite_f(g.weight_decay)) return CS_ERR_HYPERPARAM;
@@ -133,6 +146,11 @@ int check_group(const adamw_group_t& g) {
   if (g.eps < 0.0f) return CS_ERR_HYPERPARAM;
   return CS_OK;
 }
+
+}  // namespace host
+}  // namespace cs
+
+namespace {
 
 template <int G, int W>
 int launch_class(adamw_plan* p, cs::ArgClass cls, const adamw_group_t* groups,

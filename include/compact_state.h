@@ -240,6 +240,39 @@ int adamw_build_units(const int64_t *numels, int32_t n_tensors, int32_t unit_ele
                       int32_t *tensor_out, int64_t *start_out, int32_t *len_out,
                       int64_t cap, int64_t *n_units_out);
 
+/*
+ * adamw_step_noalloc -- one fused AdamW step that allocates nothing. The pages
+ * have no counterpart to this entry point; it exists for callers that cannot
+ * call cudaMalloc: an allocator or memory pool that runs the step from its own
+ * callbacks and must not re-enter the device allocator, or a runtime that
+ * hands all device memory to its own pool at start-up.
+ *   Arguments as adamw_plan_create's tensors/state_kind plus adamw_step's
+ *   groups/grad_present/step/inv_scale/found_inf/stream; every buffer is the
+ *   caller's. Work units are CS_NOALLOC_UNIT elements, as in a default plan,
+ *   so results equal adamw_step's on the same inputs.
+ * Scratch: one file-scope device array of fixed size (descriptors, units,
+ * tickets, scheduler words; about 1.3 MB), held by every GPU that loads the
+ * library until the process exits. Limits: at most CS_NOALLOC_MAX_TENSORS
+ * tensors, CS_NOALLOC_MAX_UNITS work units (2^31 elements at full units) and
+ * CS_SMALL... groups as adamw_step; beyond them it returns CS_ERR_LIMIT
+ * without touching the device.
+ * The first call on a device resolves the array's device address there (with
+ * that device current); make that first call before any stream capture.
+ * Every call shares the array and rewrites it: calls that overlap on the GPU
+ * race, so order them (one stream, or events). Calls are serialised on the
+ * host. No cudaMalloc, cudaFree or other allocating routine is called.
+ * Errors: CS_ERR_INVALID_ARGUMENT, CS_ERR_UNSUPPORTED, CS_ERR_MISALIGNED,
+ * CS_ERR_HYPERPARAM, CS_ERR_LIMIT, CS_ERR_CUDA.
+ */
+#define CS_NOALLOC_MAX_TENSORS 4096
+#define CS_NOALLOC_MAX_UNITS   65536
+#define CS_NOALLOC_UNIT        32768
+int adamw_step_noalloc(const adamw_tensor_t *tensors, int32_t n_tensors, int32_t state_kind,
+                       const adamw_group_t *groups, int32_t n_groups,
+                       const uint32_t *grad_present, int32_t *step,
+                       const float *inv_scale, const float *found_inf,
+                       struct CUstream_st *stream);
+
 /* adamw_strerror -- static string naming a status code (never NULL). */
 const char *adamw_strerror(int status);
 
