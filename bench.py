@@ -313,7 +313,8 @@ def run_native(args, wl, rank, world, dev):
     alg_bytes = elems * bpe
     peak, peak_src = hbm_peak()
     achieved = alg_bytes / (avg_kernel_ms / 1e3) / 1e9
-    traffic = committed_traffic(args.workload, state)
+    key = args.workload + (f"_{args.param_dtype}" if args.param_dtype else "")
+    traffic = committed_traffic(key, state)
     result = dict(
         value=value, ms_per_step=max_ms / K, kernel_ms_avg=avg_kernel_ms,
         kernel_ms_median=statistics.median(per), wall_s=wall, clocks=clocks,
@@ -457,6 +458,8 @@ def main(argv=None):
     ap.add_argument("--workload", default="few_large",
                     choices=["few_large", "llama3_8b", "many_small", "lora", "tiny"])
     ap.add_argument("--state", default="f32", choices=["f32", "bf16", "int8"])
+    ap.add_argument("--param-dtype", default=None, choices=["f32", "bf16", "f16"],
+                    help="override the workload's param/grad dtype")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--grad-sets", type=int, default=8)
     ap.add_argument("--e2e-steps", type=int, default=20)
@@ -469,6 +472,10 @@ def main(argv=None):
 
     rank, world, local = init_dist(args)
     wl = load_workload(args.workload)
+    if args.param_dtype:
+        import dataclasses
+        wl = dataclasses.replace(wl, param_dtype=args.param_dtype,
+                                 name=f"{wl.name}_{args.param_dtype}")
     metric = "AdamW step param-elements/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
     config = {"workload": describe(wl, args.state), "elements": wl.total_numel,
               "tensors": len(wl.tensors), "param_dtype": wl.param_dtype,

@@ -31,7 +31,7 @@ CS_MAX_GROUPS = 64
 CS_MAX_TENSORS = 245760
 CS_NOALLOC_MAX_TENSORS = 4096
 CS_NOALLOC_MAX_UNITS = 65536
-CS_NOALLOC_UNIT = 32768
+CS_NOALLOC_UNIT = 49152
 
 DTYPE_CODES = {"f32": CS_DTYPE_F32, "bf16": CS_DTYPE_BF16, "f16": CS_DTYPE_F16}
 STATE_CODES = {"f32": CS_STATE_F32, "bf16": CS_STATE_BF16, "int8": CS_STATE_INT8}

@@ -9,22 +9,30 @@
 
 namespace cs {
 
-#ifndef CS_CONSUMER_WARPS
-#define CS_CONSUMER_WARPS 16
+#ifndef CS_WARPS_ELEMENTWISE
+#define CS_WARPS_ELEMENTWISE 24   // compute warps per CTA, fp32 / bf16 moments
+#endif
+#ifndef CS_WARPS_INT8
+#define CS_WARPS_INT8 16          // compute warps per CTA, int8 moments
 #endif
 
-constexpr int kConsumerWarps = CS_CONSUMER_WARPS;      // compute warps per CTA
-constexpr int kConsumerThreads = 32 * kConsumerWarps;
-constexpr int kThreads = 32 + kConsumerThreads;        // + one producer warp
 constexpr int kDefaultUnitElems = CS_NOALLOC_UNIT;     // elements per work unit
 constexpr int kInt8Block = CS_INT8_BLOCK;
-constexpr int kStageBudget = 200 * 1024;               // dynamic shared memory for stages
+constexpr int kProducerWarps = 2;                      // tile publisher + unit fetcher
+constexpr int kStageBudget = 216 * 1024;               // dynamic shared memory for stages
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;     // 2 s bound on every wait
 
+constexpr int consumer_warps(int state_kind) {
+  return state_kind == CS_STATE_INT8 ? CS_WARPS_INT8 : CS_WARPS_ELEMENTWISE;
+}
+constexpr int block_threads(int state_kind) {
+  return 32 * (kProducerWarps + consumer_warps(state_kind));
+}
 // Elements per pipeline stage: one 4-element group per compute thread for
 // fp32/bf16 moments, one 256-element block per compute warp for int8.
 constexpr int tile_elems(int state_kind) {
-  return state_kind == CS_STATE_INT8 ? kConsumerWarps * kInt8Block : kConsumerThreads * 4;
+  return state_kind == CS_STATE_INT8 ? consumer_warps(state_kind) * kInt8Block
+                                     : consumer_warps(state_kind) * 32 * 4;
 }
 // Bytes of one pipeline stage for a state kind (params sized for fp32, the
 // widest param type, since the param type varies per tensor).
@@ -35,20 +43,22 @@ constexpr int stage_bytes(int state_kind) {
                                              2 * (tile_elems(state_kind) / kInt8Block) * 4;
 }
 constexpr int stages_for(int state_kind) {
-  return kStageBudget / ((stage_bytes(state_kind) + 127) / 128 * 128) > 8
-             ? 8
+  return kStageBudget / ((stage_bytes(state_kind) + 127) / 128 * 128) > 16
+             ? 16
              : kStageBudget / ((stage_bytes(state_kind) + 127) / 128 * 128);
 }
 static_assert(tile_elems(CS_STATE_INT8) % 1024 == 0 && tile_elems(CS_STATE_F32) % 1024 == 0,
               "tiles hold whole int8 blocks in 16-byte scale groups");
-static_assert(kDefaultUnitElems % tile_elems(CS_STATE_INT8) == 0 &&
-              kDefaultUnitElems % tile_elems(CS_STATE_F32) == 0, "units hold whole tiles");
+static_assert(block_threads(CS_STATE_F32) <= 1024 && block_threads(CS_STATE_INT8) <= 1024,
+              "threads per CTA");
+static_assert(kDefaultUnitElems % kInt8Block == 0, "units hold whole int8 blocks");
 
 // Error bits the kernel sets in the plan's error word (never traps).
 enum : uint32_t {
   kErrConsumerWait = 1u,   // a compute warp gave up waiting for a tile
   kErrProducerWait = 2u,   // the producer gave up waiting for a tile's compute
   kErrDrainWait = 4u,      // the producer gave up waiting for its own loads
+  kErrFetchWait = 8u,      // the unit fetcher gave up waiting for the publisher
 };
 // Debug flags (test hook; 0 in normal use).
 enum : uint32_t {

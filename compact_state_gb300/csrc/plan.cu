@@ -429,9 +429,14 @@ int adamw_plan_error(adamw_plan_t* p, uint32_t* out_flags) {
   if (cudaDeviceSynchronize() != cudaSuccess) return CS_ERR_CUDA;
   if (cudaMemcpy(&v, p->d_sched + 2, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
     return CS_ERR_CUDA;
-  const uint32_t zero = 0;
-  if (cudaMemcpy(p->d_sched + 2, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
-    return CS_ERR_CUDA;
+  if (v != 0) {
+    // a step that gave up may leave queue words and commit tickets behind:
+    // clear them together with the error word
+    const size_t bytes = reinterpret_cast<char*>(p->d_sched) + 256 -
+                         reinterpret_cast<char*>(p->d_commit);
+    if (cudaMemset(p->d_commit, 0, bytes) != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+      return CS_ERR_CUDA;
+  }
   *out_flags = v;
   return CS_OK;
 }
@@ -455,7 +460,7 @@ int adamw_plan_info(const adamw_plan_t* p, adamw_plan_info_t* out) {
   out->state_kind = p->state_kind;
   out->unit_elems = p->unit_elems;
   out->grid_blocks = p->grid[cs::kClassSmall];
-  out->block_threads = cs::kThreads;
+  out->block_threads = cs::block_threads(p->state_kind);
   out->device = p->device;
   return CS_OK;
 }

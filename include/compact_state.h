@@ -130,7 +130,7 @@ typedef struct adamw_plan_info_t {
  *   tensors     host array [n_tensors], read only during the call.
  *   n_tensors   1 .. CS_MAX_TENSORS.
  *   state_kind  CS_STATE_*; one kind for all tensors of the plan.
- *   unit_elems  elements per work unit; 0 picks the default (32768). Must be
+ *   unit_elems  elements per work unit; 0 picks the default (49152). Must be
  *               a positive multiple of 256 otherwise.
  *   out_plan    host out-parameter; set to NULL on failure.
  * Allocates device memory (descriptors 64 B/tensor, units 16 B/unit,
@@ -188,9 +188,13 @@ int adamw_plan_set_grads(adamw_plan_t *plan, const void *const *grads,
  * runs out sets a bit here and that CTA winds down without touching its
  * remaining tiles; nothing traps and the CUDA context stays usable. Bits:
  * 1 a compute warp gave up waiting for a tile, 2 the producer gave up waiting
- * for a tile's compute, 4 the producer gave up waiting for its own loads.
- * 0 means every step since the last call ran to completion. Synchronises the
- * device. Errors: CS_ERR_INVALID_ARGUMENT, CS_ERR_WRONG_DEVICE, CS_ERR_CUDA.
+ * for a tile's compute, 4 the producer gave up waiting for its own loads,
+ * 8 the unit fetcher gave up waiting for the producer.
+ * 0 means every step since the last call ran to completion. A nonzero read
+ * also clears the plan's work queue and commit counters, which a step that
+ * gave up leaves behind, so the next step starts clean (the steps that gave up
+ * are not redone). Synchronises the device.
+ * Errors: CS_ERR_INVALID_ARGUMENT, CS_ERR_WRONG_DEVICE, CS_ERR_CUDA.
  */
 int adamw_plan_error(adamw_plan_t *plan, uint32_t *out_flags);
 
@@ -253,7 +257,7 @@ int adamw_build_units(const int64_t *numels, int32_t n_tensors, int32_t unit_ele
  * Scratch: one file-scope device array of fixed size (descriptors, units,
  * tickets, scheduler words; about 1.3 MB), held by every GPU that loads the
  * library until the process exits. Limits: at most CS_NOALLOC_MAX_TENSORS
- * tensors, CS_NOALLOC_MAX_UNITS work units (2^31 elements at full units) and
+ * tensors, CS_NOALLOC_MAX_UNITS work units (3.2e9 elements at full units) and
  * CS_SMALL... groups as adamw_step; beyond them it returns CS_ERR_LIMIT
  * without touching the device.
  * The first call on a device resolves the array's device address there (with
@@ -266,7 +270,7 @@ int adamw_build_units(const int64_t *numels, int32_t n_tensors, int32_t unit_ele
  */
 #define CS_NOALLOC_MAX_TENSORS 4096
 #define CS_NOALLOC_MAX_UNITS   65536
-#define CS_NOALLOC_UNIT        32768
+#define CS_NOALLOC_UNIT        49152
 int adamw_step_noalloc(const adamw_tensor_t *tensors, int32_t n_tensors, int32_t state_kind,
                        const adamw_group_t *groups, int32_t n_groups,
                        const uint32_t *grad_present, int32_t *step,
