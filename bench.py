@@ -274,9 +274,22 @@ def run_native(args, wl, rank, world, dev):
     L = cs.lib()
     hs = stream.cuda_stream
 
+    pro = torch.zeros(3, dtype=torch.float32, device=dev)   # found_inf, norm, scale
+
     def one(k):
-        rc = L.adamw_step(plans[k % len(plans)].handle, groups, ng, None,
-                          st.step.data_ptr(), inv.data_ptr(), fi.data_ptr(), hs)
+        plan = plans[k % len(plans)].handle
+        if args.prologue is not None:
+            # unscale, non-finite check and clip first; the step takes their result
+            rc = L.adamw_grad_prologue(plan, None, inv.data_ptr(), float(args.prologue),
+                                       pro.data_ptr(), pro.data_ptr() + 4,
+                                       pro.data_ptr() + 8, hs)
+            if rc:
+                raise cs.CompactStateError(rc, "adamw_grad_prologue")
+            rc = L.adamw_step(plan, groups, ng, None, st.step.data_ptr(), pro.data_ptr() + 8,
+                              pro.data_ptr(), hs)
+        else:
+            rc = L.adamw_step(plan, groups, ng, None, st.step.data_ptr(), inv.data_ptr(),
+                              fi.data_ptr(), hs)
         if rc:
             raise cs.CompactStateError(rc, "adamw_step")
 
@@ -310,6 +323,8 @@ def run_native(args, wl, rank, world, dev):
     value = world * elems * K / (max_ms / 1e3)
     avg_kernel_ms = sum(per) / len(per)
     bpe = BYTES_PER_ELEM[(wl.param_dtype, state)]
+    if args.prologue is not None:
+        bpe += 4 if wl.param_dtype == "f32" else 2     # the prologue reads the grads once more
     alg_bytes = elems * bpe
     peak, peak_src = hbm_peak()
     achieved = alg_bytes / (avg_kernel_ms / 1e3) / 1e9
@@ -461,6 +476,9 @@ def main(argv=None):
     ap.add_argument("--param-dtype", default=None, choices=["f32", "bf16", "f16"],
                     help="override the workload's param/grad dtype")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--prologue", type=float, default=None, metavar="MAX_NORM",
+                    help="run the gradient prologue (non-finite check, norm, clip at "
+                         "MAX_NORM) before every step and time both")
     ap.add_argument("--grad-sets", type=int, default=8)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--e2e-chunk", type=int, default=1 << 22)
@@ -516,7 +534,8 @@ def main(argv=None):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded normal params and grads)", "config": config,
             "roofline": res["roofline"], "clocks": res["clocks"],
-            "e2e": res.get("e2e"), "gpu_launches": args.steps,
+            "e2e": res.get("e2e"),
+            "gpu_launches": args.steps * (2 if args.prologue is not None else 1),
             "kernel_ms_avg": res["kernel_ms_avg"], "kernel_ms_median": res["kernel_ms_median"],
             "grad_sets": res["grad_sets"], "cpu_baseline": cb}
     print(json.dumps(line), flush=True)

@@ -68,7 +68,8 @@ class CompactStateError(RuntimeError):
 _LIB = None
 EXPORTS = ("adamw_plan_create", "adamw_step", "adamw_plan_set_grads", "adamw_plan_info",
            "adamw_plan_destroy", "adamw_state_bytes", "adamw_build_units", "adamw_strerror",
-           "adamw_plan_error", "adamw_plan_set_debug", "adamw_step_noalloc")
+           "adamw_plan_error", "adamw_plan_set_debug", "adamw_step_noalloc",
+           "adamw_grad_prologue")
 
 
 def lib() -> ctypes.CDLL:
@@ -98,6 +99,8 @@ def lib() -> ctypes.CDLL:
     L.adamw_step_noalloc.argtypes = [ctypes.POINTER(adamw_tensor_t), i32, i32,
                                      ctypes.POINTER(adamw_group_t), i32,
                                      ctypes.POINTER(ctypes.c_uint32), vp, vp, vp, vp]
+    L.adamw_grad_prologue.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp, ctypes.c_float,
+                                      vp, vp, vp, vp]
     L.adamw_strerror.argtypes = [ctypes.c_int]
     L.adamw_strerror.restype = ctypes.c_char_p
     for name in EXPORTS:
@@ -236,6 +239,19 @@ def adamw_step_noalloc(tensors: Sequence[adamw_tensor_t], state_kind, groups,
                                   _ptr(step), _ptr(inv_scale), _ptr(found_inf),
                                   _stream(stream))
     _check(rc, "adamw_step_noalloc")
+
+
+def adamw_grad_prologue(plan: Plan, grad_present=None, inv_scale=None, max_norm: float = 0.0,
+                        found_inf_out=None, grad_norm_out=None, scale_out=None,
+                        stream=None) -> None:
+    """Enqueue the gradient checks before a step: non-finite flag, global L2
+    norm and clip factor into device fp32 scalars (asynchronous)."""
+    if grad_present is not None and not isinstance(grad_present, ctypes.Array):
+        grad_present = pack_present(grad_present, plan.n_tensors)
+    rc = lib().adamw_grad_prologue(plan.handle, grad_present, _ptr(inv_scale),
+                                   float(max_norm), _ptr(found_inf_out), _ptr(grad_norm_out),
+                                   _ptr(scale_out), _stream(stream))
+    _check(rc, "adamw_grad_prologue")
 
 
 def adamw_plan_set_grads(plan: Plan, grads: Sequence, stream=None) -> None:

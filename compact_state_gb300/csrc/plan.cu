@@ -8,6 +8,7 @@
 #include <vector>
 
 #include "adamw_internal.h"
+#include "prologue.h"
 
 using cs::TensorDesc;
 using cs::WorkUnit;
@@ -23,11 +24,14 @@ struct adamw_plan {
   int64_t total_numel = 0;
   int64_t device_bytes = 0;
   int grid[3] = {0, 0, 0};        // persistent grid per argument class
-  void* dev = nullptr;            // one allocation: descs | units | commit | sched
+  int pgrid[3] = {0, 0, 0};       // gradient prologue: one wave of resident blocks
+  void* dev = nullptr;            // one allocation: descs | units | commit | sched | prologue
   TensorDesc* d_descs = nullptr;
   WorkUnit* d_units = nullptr;
   uint32_t* d_commit = nullptr;
   uint32_t* d_sched = nullptr;     // [0] next unit, [1] CTAs done, [2] error bits
+  double* d_partial = nullptr;     // gradient prologue: per-block sums of squares
+  uint32_t* d_pwords = nullptr;    // gradient prologue: [0] blocks done, [1] non-finite
   uint64_t wait_ns = cs::kDefaultWaitNs;
   uint32_t debug = 0;
   std::vector<TensorDesc> h_descs;
@@ -182,6 +186,39 @@ int launch_class(adamw_plan* p, cs::ArgClass cls, const adamw_group_t* groups,
 
 }  // namespace
 
+namespace {
+
+template <int W>
+int launch_prologue_class(adamw_plan* p, cs::ArgClass cls, const uint32_t* present,
+                          const float* inv_scale, float max_norm, float* found_inf_out,
+                          float* norm_out, float* scale_out, cudaStream_t stream) {
+  cs::PrologueArgs<W> a;
+  std::memset(&a, 0, sizeof(a));
+  a.descs = p->d_descs;
+  a.units = p->d_units;
+  a.inv_scale = inv_scale;
+  a.found_inf_out = found_inf_out;
+  a.norm_out = norm_out;
+  a.scale_out = scale_out;
+  a.partial = p->d_partial;
+  a.words = p->d_pwords;
+  a.max_norm = max_norm;
+  a.n_units = static_cast<int32_t>(p->n_units);
+  a.pieces_per_unit = (p->unit_elems + cs::kProloguePiece - 1) / cs::kProloguePiece;
+  if (present) {
+    a.all_present = 0;
+    std::memcpy(a.present, present, sizeof(uint32_t) * ((p->n_tensors + 31) / 32));
+  } else {
+    a.all_present = 1;
+  }
+  const int64_t items = static_cast<int64_t>(a.n_units) * a.pieces_per_unit;
+  const int grid = static_cast<int>(std::max<int64_t>(
+      1, std::min<int64_t>(items, p->pgrid[cls])));
+  return cs::launch_prologue(cls, &a, grid, stream) == cudaSuccess ? CS_OK : CS_ERR_CUDA;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* adamw_strerror(int status) {
@@ -303,13 +340,19 @@ int adamw_plan_create(const adamw_tensor_t* tensors, int32_t n_tensors, int32_t 
       const int64_t want = static_cast<int64_t>(per_sm) * p->sm_count;
       // never more CTAs than units (at least one)
       p->grid[c] = static_cast<int>(std::max<int64_t>(1, std::min<int64_t>(want, p->n_units)));
+      if (cs::prologue_occupancy(static_cast<cs::ArgClass>(c), &per_sm) != cudaSuccess || per_sm <= 0) {
+        delete p; return CS_ERR_CUDA;
+      }
+      p->pgrid[c] = static_cast<int>(
+          std::min<int64_t>(static_cast<int64_t>(per_sm) * p->sm_count, cs::kPrologueMaxBlocks));
     }
 
     const size_t b_desc = sizeof(TensorDesc) * n_tensors;
     const size_t b_units = sizeof(WorkUnit) * std::max<size_t>(units.size(), 1);
     const size_t b_commit = ((sizeof(uint32_t) * n_tensors + 255) / 256) * 256;
     const size_t b_sched = 256;
-    const size_t total = b_desc + b_units + b_commit + b_sched;
+    const size_t b_pro = sizeof(double) * cs::kPrologueMaxBlocks + 256;
+    const size_t total = b_desc + b_units + b_commit + b_sched + b_pro;
     if (cudaMalloc(&p->dev, total) != cudaSuccess) {
       cudaGetLastError();
       delete p;
@@ -321,11 +364,14 @@ int adamw_plan_create(const adamw_tensor_t* tensors, int32_t n_tensors, int32_t 
     p->d_units = reinterpret_cast<WorkUnit*>(base + b_desc);
     p->d_commit = reinterpret_cast<uint32_t*>(base + b_desc + b_units);
     p->d_sched = reinterpret_cast<uint32_t*>(base + b_desc + b_units + b_commit);
+    p->d_partial = reinterpret_cast<double*>(base + b_desc + b_units + b_commit + b_sched);
+    p->d_pwords = reinterpret_cast<uint32_t*>(base + b_desc + b_units + b_commit + b_sched +
+                                              sizeof(double) * cs::kPrologueMaxBlocks);
     bool ok = cudaMemcpy(p->d_descs, p->h_descs.data(), b_desc, cudaMemcpyHostToDevice) == cudaSuccess;
     if (ok && !units.empty())
       ok = cudaMemcpy(p->d_units, units.data(), sizeof(WorkUnit) * units.size(),
                       cudaMemcpyHostToDevice) == cudaSuccess;
-    ok = ok && cudaMemset(p->d_commit, 0, b_commit + b_sched) == cudaSuccess;
+    ok = ok && cudaMemset(p->d_commit, 0, b_commit + b_sched + b_pro) == cudaSuccess;
     ok = ok && cudaDeviceSynchronize() == cudaSuccess;
     if (!ok) {
       cudaFree(p->dev);
@@ -376,6 +422,29 @@ int adamw_step(adamw_plan_t* p, const adamw_group_t* groups, int32_t n_groups,
       return launch_class<cs::kLargeGroups, cs::kLargeWords>(p, cls, groups, n_groups, grad_present,
                                                              step, inv_scale, found_inf, s);
   }
+}
+
+int adamw_grad_prologue(adamw_plan_t* p, const uint32_t* grad_present, const float* inv_scale,
+                        float max_norm, float* found_inf_out, float* grad_norm_out,
+                        float* scale_out, struct CUstream_st* stream) {
+  if (!p || !found_inf_out || !scale_out) return CS_ERR_INVALID_ARGUMENT;
+  if (!std::isfinite(max_norm)) return CS_ERR_HYPERPARAM;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CS_ERR_CUDA;
+  if (dev != p->device) return CS_ERR_WRONG_DEVICE;
+  const int32_t need = grad_present ? p->n_tensors : 0;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (need <= cs::kSmallWords * 32)
+    return launch_prologue_class<cs::kSmallWords>(p, cs::kClassSmall, grad_present, inv_scale,
+                                                  max_norm, found_inf_out, grad_norm_out,
+                                                  scale_out, s);
+  if (need <= cs::kMidWords * 32)
+    return launch_prologue_class<cs::kMidWords>(p, cs::kClassMid, grad_present, inv_scale,
+                                                max_norm, found_inf_out, grad_norm_out,
+                                                scale_out, s);
+  return launch_prologue_class<cs::kLargeWords>(p, cs::kClassLarge, grad_present, inv_scale,
+                                                max_norm, found_inf_out, grad_norm_out, scale_out,
+                                                s);
 }
 
 int adamw_plan_set_grads(adamw_plan_t* p, const void* const* grads, struct CUstream_st* stream) {

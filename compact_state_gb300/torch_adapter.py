@@ -10,8 +10,8 @@ from typing import List, Optional, Sequence
 
 import torch
 
-from ._binding import (CS_INT8_BLOCK, Plan, adamw_plan_create, adamw_plan_set_grads,
-                       adamw_step, pack_present, tensor_desc)
+from ._binding import (CS_INT8_BLOCK, Plan, adamw_grad_prologue, adamw_plan_create,
+                       adamw_plan_set_grads, adamw_step, pack_present, tensor_desc)
 
 STATE_TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "int8": torch.int8}
 
@@ -64,6 +64,18 @@ class AdamWState:
         """One optimizer step (asynchronous on ``stream``)."""
         bits = None if present is None else pack_present(present, len(self.params))
         adamw_step(self.plan, groups, bits, self.step, inv_scale, found_inf, stream)
+
+    def prologue(self, present=None, inv_scale=None, max_norm: float = 0.0, stream=None):
+        """Non-finite flag, global norm and clip factor of this step's grads, as
+        device fp32 tensors (found_inf, norm, scale); pass found_inf and scale
+        to run() as found_inf and inv_scale."""
+        dev = self.step.device
+        if not hasattr(self, "_pro_out"):
+            self._pro_out = torch.zeros(3, dtype=torch.float32, device=dev)
+        o = self._pro_out
+        bits = None if present is None else pack_present(present, len(self.params))
+        adamw_grad_prologue(self.plan, bits, inv_scale, max_norm, o[0:1], o[1:2], o[2:3], stream)
+        return o[0:1], o[1:2], o[2:3]
 
     def set_grads(self, grads: Sequence[torch.Tensor], stream=None) -> None:
         self.grads = list(grads)

@@ -134,7 +134,8 @@ typedef struct adamw_plan_info_t {
  *               a positive multiple of 256 otherwise.
  *   out_plan    host out-parameter; set to NULL on failure.
  * Allocates device memory (descriptors 64 B/tensor, units 16 B/unit,
- * a 4 B/tensor commit counter, two scheduler words and an error word).
+ * a 4 B/tensor commit counter, two scheduler words, an error word and 16 KB
+ * of partial sums for adamw_grad_prologue).
  * Synchronous.
  * Errors: CS_ERR_INVALID_ARGUMENT, CS_ERR_UNSUPPORTED, CS_ERR_MISALIGNED,
  * CS_ERR_LIMIT, CS_ERR_OUT_OF_MEMORY, CS_ERR_CUDA.
@@ -168,6 +169,35 @@ int adamw_step(adamw_plan_t *plan, const adamw_group_t *groups, int32_t n_groups
                const uint32_t *grad_present, int32_t *step,
                const float *inv_scale, const float *found_inf,
                struct CUstream_st *stream);
+
+/*
+ * adamw_grad_prologue -- the gradient checks that precede the update, in one
+ * pass over every present gradient of the plan, on the device: unscale,
+ * non-finite check, global L2 norm and clip factor ("Fused Optimizers and
+ * State Precision", section 06: unscale, check for non-finite values and clip
+ * before updating; the Apex FusedAdam capturable path, section 4.3, and
+ * FusedLAMB's global gradient norm, section 5.3).
+ *   grad_present   as for adamw_step (host bitmask, NULL = all present).
+ *   inv_scale      device fp32 scalar multiplied into every gradient; NULL = 1.
+ *   max_norm       clip threshold; <= 0 disables clipping; must be finite.
+ *   found_inf_out  device fp32: 1 if any g*inv_scale (fp32) of a present
+ *                  tensor is NaN or infinite, else 0.
+ *   grad_norm_out  device fp32 (NULL allowed): sqrt(sum (g*inv_scale)^2) over
+ *                  present tensors; NaN when found_inf_out is 1.
+ *   scale_out      device fp32: inv_scale * min(1, max_norm/(norm + 1e-6)),
+ *                  or inv_scale when not clipping or when found_inf_out is 1.
+ * Passing found_inf_out and scale_out to adamw_step as its found_inf and
+ * inv_scale runs unscale, check, clip and update in that order with no host
+ * sync. Squares are summed in fp32 with compensation per thread and in fp64
+ * across blocks, in a fixed order (the result does not depend on timing).
+ * Asynchronous on `stream`, allocates nothing. Must not overlap another
+ * prologue of the same plan.
+ * Errors: CS_ERR_INVALID_ARGUMENT, CS_ERR_HYPERPARAM (non-finite max_norm),
+ * CS_ERR_WRONG_DEVICE, CS_ERR_CUDA.
+ */
+int adamw_grad_prologue(adamw_plan_t *plan, const uint32_t *grad_present,
+                        const float *inv_scale, float max_norm, float *found_inf_out,
+                        float *grad_norm_out, float *scale_out, struct CUstream_st *stream);
 
 /*
  * adamw_plan_set_grads -- replace the gradient pointers of every tensor (for

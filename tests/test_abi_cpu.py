@@ -45,7 +45,7 @@ def _header_defines():
 
 def test_exports_every_declared_symbol(cs):
     declared = _header_functions()
-    assert len(declared) == 11, declared
+    assert len(declared) == 12, declared
     assert sorted(cs.EXPORTS) == declared
     L = cs.lib()
     for name in declared:
@@ -159,6 +159,7 @@ def test_step_rejects_null_plan(cs):
     assert cs.lib().adamw_plan_info(None, None) == -1
     assert cs.lib().adamw_plan_error(None, None) == -1
     assert cs.lib().adamw_plan_set_debug(None, 0, 0) == -1
+    assert cs.lib().adamw_grad_prologue(None, None, None, 1.0, 0x10, None, 0x20, None) == -1
     assert cs.lib().adamw_plan_destroy(None) == 0
 
 
