@@ -32,6 +32,15 @@ Readings (the pages leave these open):
   moments are rounded afterwards.
 * Stored values are rounded once, from float64, on every store: theta to the
   param format, moments to the state format (``formats``, ``int8_block``).
+
+fp32 master weights (the Apex fused-optimizers guide, FusedAdam
+``master_weights``, sections 4.2 and 4.3): a 16-bit model parameter may carry an
+fp32 master copy. The update then works on the master, not on the 16-bit
+value: the new theta is stored to the master in fp32, and the model parameter
+becomes the master rounded to its 16-bit format (round to nearest even), so
+updates smaller than half a 16-bit ulp still accumulate. The gradient stays in
+the model's format. Reading: the master starts as the exact fp32 value of the
+model parameter, as Apex creates it from the model's parameters.
 """
 from __future__ import annotations
 
@@ -76,12 +85,17 @@ class TensorState:
     v_scale: Optional[np.ndarray] = None
     step: int = 0
     group: int = 0
+    master: Optional[np.ndarray] = None   # fp32 master weights (float64 values)
 
     def copy(self) -> "TensorState":
         c = lambda a: None if a is None else np.array(a, copy=True)
         return TensorState(c(self.theta), self.param_fmt, self.state_kind,
                            c(self.m), c(self.v), c(self.m_scale), c(self.v_scale),
-                           int(self.step), int(self.group))
+                           int(self.step), int(self.group), c(self.master))
+
+    def weights(self) -> np.ndarray:
+        """The values the update works on: the master when there is one."""
+        return self.theta if self.master is None else self.master
 
     # -- decode / encode ---------------------------------------------------
     def moments(self):
@@ -92,7 +106,11 @@ class TensorState:
                 np.asarray(self.v, dtype=np.float64))
 
     def store(self, theta, m, v) -> None:
-        self.theta = round_to(theta, self.param_fmt)
+        if self.master is None:
+            self.theta = round_to(theta, self.param_fmt)
+        else:
+            self.master = round_to(theta, "f32")
+            self.theta = round_to(self.master, self.param_fmt)
         if self.state_kind == "int8":
             self.m, self.m_scale = int8_block.encode(m)
             self.v, self.v_scale = int8_block.encode(v)
@@ -102,17 +120,19 @@ class TensorState:
 
 
 def new_state(theta, param_fmt: str, state_kind: str, group: int = 0,
-              step: int = 0) -> TensorState:
-    """Zero moments (the optimizer's lazy zero initialisation)."""
+              step: int = 0, master: bool = False) -> TensorState:
+    """Zero moments (the optimizer's lazy zero initialisation); with
+    ``master``, an fp32 master equal to the (16-bit) parameter's value."""
     theta = round_to(np.asarray(theta, dtype=np.float64).reshape(-1), param_fmt)
     n = theta.size
+    mw = np.array(theta, copy=True) if master else None
     if state_kind == "int8":
         nb = int8_block.n_blocks(n)
         return TensorState(theta, param_fmt, state_kind, np.zeros(n, np.int8),
                            np.zeros(n, np.int8), np.zeros(nb, np.float32),
-                           np.zeros(nb, np.float32), step, group)
+                           np.zeros(nb, np.float32), step, group, mw)
     return TensorState(theta, param_fmt, state_kind, np.zeros(n), np.zeros(n),
-                       None, None, step, group)
+                       None, None, step, group, mw)
 
 
 def _hyper(group):
@@ -139,7 +159,7 @@ def oracle_step(states: List[TensorState], groups: Sequence,
         t = st.step + 1
         m, v = st.moments()
         g = np.asarray(g, dtype=np.float64).reshape(-1) * float(inv_scale)
-        theta, m, v = adamw_update(st.theta, g, m, v, t, lr, b1, b2, eps, wd)
+        theta, m, v = adamw_update(st.weights(), g, m, v, t, lr, b1, b2, eps, wd)
         st.store(theta, m, v)
         st.step = t
 
@@ -171,6 +191,6 @@ def oracle_step_three_loops(states: List[TensorState], groups: Sequence,
         t = st.step + 1
         m_hat = m / (1.0 - b1 ** t)
         v_hat = v / (1.0 - b2 ** t)
-        theta = st.theta * (1.0 - lr * wd) - lr * m_hat / (np.sqrt(v_hat) + eps)
+        theta = st.weights() * (1.0 - lr * wd) - lr * m_hat / (np.sqrt(v_hat) + eps)
         st.store(theta, m, v)
         st.step = t
