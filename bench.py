@@ -41,6 +41,13 @@ BYTES_PER_ELEM = {  # (param dtype, state kind) -> read + write bytes per elemen
     ("f32", "int8"): 16.0625, ("bf16", "int8"): 10.0625, ("f16", "int8"): 10.0625,
 }
 FALLBACK_HBM_GBS = 6800.0
+
+
+def bytes_per_elem(param_dtype: str, state: str, master: bool = False) -> float:
+    """Algorithmic bytes per element of one step. With fp32 master weights
+    theta is read from the master (4 B instead of the 16-bit param's 2) and
+    written to both (4 + 2 B instead of 2): 6 B more."""
+    return BYTES_PER_ELEM[(param_dtype, state)] + (6 if master else 0)
 KERNEL_SRCS = [os.path.join(ROOT, "compact_state_gb300", "csrc", f)
                for f in ("adamw_kernels.cu", "adamw_internal.h")]
 
@@ -164,25 +171,26 @@ def committed_traffic(workload: str, state: str):
 
 
 # ------------------------------------------------------------------ oracle
-def _oracle_setup(wl, state, n):
+def _oracle_setup(wl, state, n, master=False):
     import numpy as np
     from oracle.adamw import new_state
     big = max(range(len(wl.tensors)), key=lambda i: wl.tensors[i].numel)
     n = min(wl.tensors[big].numel, n)
     rng = np.random.default_rng(0)
     st = [new_state(rng.normal(0, wl.param_std, n), wl.param_dtype, state,
-                    group=wl.tensors[big].group)]
+                    group=wl.tensors[big].group, master=master)]
     groups = [dict(lr=x.lr, beta1=x.beta1, beta2=x.beta2, eps=x.eps,
                    weight_decay=x.weight_decay) for x in wl.groups]
     grads = [rng.normal(0, wl.grad_std, n) * wl.grad_prescale for _ in range(2)]
     return st, groups, grads, n, wl.tensors[big].name
 
 
-def cpu_baseline(wl, state: str, budget_s: float = 12.0, n_max: int = 1 << 21) -> dict:
+def cpu_baseline(wl, state: str, budget_s: float = 12.0, n_max: int = 1 << 21,
+                 master: bool = False) -> dict:
     """The oracle, as it is, on a bounded sample: a contiguous slice of the
     workload's largest tensor, stepped repeatedly for about ``budget_s``."""
     from oracle.adamw import oracle_step
-    st, groups, grads, n, name = _oracle_setup(wl, state, n_max)
+    st, groups, grads, n, name = _oracle_setup(wl, state, n_max, master)
     steps = 0
     t0 = time.perf_counter()
     while True:
@@ -193,15 +201,16 @@ def cpu_baseline(wl, state: str, budget_s: float = 12.0, n_max: int = 1 << 21) -
             break
     return {"value": steps * n / el, "unit": "param-elements/s", "cores": 1,
             "kind": "oracle",
-            "sample": f"{n} elements of tensor '{name}' ({wl.param_dtype} params, "
-                      f"{state} state), {steps} steps in {el:.1f} s, numpy float64, "
+            "sample": f"{n} elements of tensor '{name}' ({wl.param_dtype} params"
+                      f"{' with fp32 master' if master else ''}, {state} state), {steps} steps in {el:.1f} s, numpy float64, "
                       f"one thread"}
 
 
-def reference_arm(wl, state: str, steps: int, warmup: int, n: int = 1 << 18) -> dict:
+def reference_arm(wl, state: str, steps: int, warmup: int, n: int = 1 << 18,
+                  master: bool = False) -> dict:
     """W untimed + K timed oracle steps, each over a bounded sample of n elements."""
     from oracle.adamw import oracle_step
-    st, groups, grads, n, name = _oracle_setup(wl, state, n)
+    st, groups, grads, n, name = _oracle_setup(wl, state, n, master)
     for k in range(warmup):
         oracle_step(st, groups, [grads[k % 2]], inv_scale=wl.inv_scale)
     t0 = time.perf_counter()
@@ -211,11 +220,11 @@ def reference_arm(wl, state: str, steps: int, warmup: int, n: int = 1 << 18) -> 
     return {"value": steps * n / el, "unit": "param-elements/s", "cores": 1,
             "kind": "oracle", "elapsed_s": el,
             "sample": f"each step: {n} elements of tensor '{name}' ({wl.param_dtype} "
-                      f"params, {state} state), numpy float64, one thread"}
+                      f"params{' with fp32 master' if master else ''}, {state} state), numpy float64, one thread"}
 
 
 # ------------------------------------------------------------------ GPU arm
-def alloc_state(wl, state, dev):
+def alloc_state(wl, state, dev, master=False):
     import torch
     import workloads
     from compact_state_gb300.torch_adapter import AdamWState
@@ -226,7 +235,7 @@ def alloc_state(wl, state, dev):
         p.copy_(workloads.init_param(wl, i, device=dev).reshape(-1))
         params.append(p)
     grads = [torch.empty_like(p) for p in params]
-    st = AdamWState(params, grads, state, [t.group for t in wl.tensors])
+    st = AdamWState(params, grads, state, [t.group for t in wl.tensors], master=master)
     return st
 
 
@@ -251,7 +260,7 @@ def run_native(args, wl, rank, world, dev):
     import compact_state_gb300 as cs
     from compact_state_gb300 import tensor_desc
     state = args.state
-    st = alloc_state(wl, state, dev)
+    st = alloc_state(wl, state, dev, args.master)
     plan_info = cs.adamw_plan_info(st.plan)
     # grad buffers: fresh seeded grads per step, cycling through a pool
     per_set = sum(g.numel() * g.element_size() for g in st.grads)
@@ -261,9 +270,9 @@ def run_native(args, wl, rank, world, dev):
     # one plan per grad set (descriptors hold grad pointers)
     plans = [st.plan]
     for gs in sets[1:]:
-        descs = [tensor_desc(p, g, m, v, ms, vs, group=t.group)
-                 for p, g, m, v, ms, vs, t in zip(st.params, gs, st.m, st.v, st.m_scale,
-                                                  st.v_scale, wl.tensors)]
+        descs = [tensor_desc(p, g, m, v, ms, vs, group=t.group, master=mw)
+                 for p, g, m, v, ms, vs, mw, t in zip(st.params, gs, st.m, st.v, st.m_scale,
+                                                      st.v_scale, st.master, wl.tensors)]
         plans.append(cs.adamw_plan_create(descs, state, 0))
     groups = cs.groups_array([dict(lr=g.lr, beta1=g.beta1, beta2=g.beta2, eps=g.eps,
                                    weight_decay=g.weight_decay) for g in wl.groups])
@@ -322,13 +331,14 @@ def run_native(args, wl, rank, world, dev):
     elems = wl.total_numel
     value = world * elems * K / (max_ms / 1e3)
     avg_kernel_ms = sum(per) / len(per)
-    bpe = BYTES_PER_ELEM[(wl.param_dtype, state)]
+    bpe = bytes_per_elem(wl.param_dtype, state, args.master)
     if args.prologue is not None:
         bpe += 4 if wl.param_dtype == "f32" else 2     # the prologue reads the grads once more
     alg_bytes = elems * bpe
     peak, peak_src = hbm_peak()
     achieved = alg_bytes / (avg_kernel_ms / 1e3) / 1e9
-    key = args.workload + (f"_{args.param_dtype}" if args.param_dtype else "")
+    key = (args.workload + (f"_{args.param_dtype}" if args.param_dtype else "")
+           + ("_master" if args.master else ""))
     traffic = committed_traffic(key, state)
     result = dict(
         value=value, ms_per_step=max_ms / K, kernel_ms_avg=avg_kernel_ms,
@@ -357,30 +367,34 @@ def run_e2e(args, wl, st, groups, ng, dev, world):
     import compact_state_gb300 as cs
     from compact_state_gb300 import tensor_desc
     chunk = max(256, (args.e2e_chunk // 256) * 256)
-    chunks = []        # (device views..., host views...)
+    chunks = []        # (tensor, device views: param, grad, m, v, m_scale, v_scale, master)
     for i in range(len(st.params)):
         n = st.params[i].numel()
         for c0 in range(0, max(n, 1), chunk):
             c1 = min(n, c0 + chunk)
-            dv = [st.params[i][c0:c1], st.grads[i][c0:c1], st.m[i][c0:c1], st.v[i][c0:c1]]
-            if st.m_scale[i] is not None:
-                b0, b1 = c0 // 256, -(-c1 // 256)
-                dv += [st.m_scale[i][b0:b1], st.v_scale[i][b0:b1]]
+            b0, b1 = c0 // 256, -(-c1 // 256)
+            sl = lambda x, a, b: None if x is None else x[a:b]
+            dv = [st.params[i][c0:c1], st.grads[i][c0:c1], st.m[i][c0:c1], st.v[i][c0:c1],
+                  sl(st.m_scale[i], b0, b1), sl(st.v_scale[i], b0, b1),
+                  sl(st.master[i], c0, c1)]
             chunks.append((i, dv))
-    host = [[d.detach().to("cpu").pin_memory() for d in dv] for _, dv in chunks]
+    host = [[None if d is None else d.detach().to("cpu").pin_memory() for d in dv]
+            for _, dv in chunks]
     plans = []
     for (i, dv) in chunks:
-        ms = dv[4] if len(dv) > 4 else None
-        vs = dv[5] if len(dv) > 4 else None
         plans.append(cs.adamw_plan_create(
-            [tensor_desc(dv[0], dv[1], dv[2], dv[3], ms, vs, group=wl.tensors[i].group)],
-            args.state, 0))
+            [tensor_desc(dv[0], dv[1], dv[2], dv[3], dv[4], dv[5], group=wl.tensors[i].group,
+                         master=dv[6])], args.state, 0))
     steps = torch.zeros(len(chunks), dtype=torch.int32, device=dev)
     inv = torch.tensor([wl.inv_scale], dtype=torch.float32, device=dev)
-    out_idx = lambda dv: [0, 2, 3] + ([4, 5] if len(dv) > 4 else [])
-    h2d = sum(h.numel() * h.element_size() for hb in host for h in hb)
-    d2h = sum(host[c][j].numel() * host[c][j].element_size()
-              for c, (_, dv) in enumerate(chunks) for j in out_idx(dv))
+    # in: what the step reads (theta from the master when there is one); out:
+    # what it writes
+    in_idx = lambda dv: [j for j in ([1, 2, 3, 4, 5, 6] if dv[6] is not None
+                                     else [0, 1, 2, 3, 4, 5]) if dv[j] is not None]
+    out_idx = lambda dv: [j for j in (0, 2, 3, 4, 5, 6) if dv[j] is not None]
+    nbytes = lambda h: h.numel() * h.element_size()
+    h2d = sum(nbytes(host[c][j]) for c, (_, dv) in enumerate(chunks) for j in in_idx(dv))
+    d2h = sum(nbytes(host[c][j]) for c, (_, dv) in enumerate(chunks) for j in out_idx(dv))
     s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
     ev_in = [torch.cuda.Event() for _ in chunks]
     ev_cmp = [torch.cuda.Event() for _ in chunks]
@@ -393,8 +407,8 @@ def run_e2e(args, wl, st, groups, ng, dev, world):
             if not first[0]:
                 s_in.wait_event(ev_out[c])
             with torch.cuda.stream(s_in):
-                for d, h in zip(dv, host[c]):
-                    d.copy_(h, non_blocking=True)
+                for j in in_idx(dv):
+                    dv[j].copy_(host[c][j], non_blocking=True)
                 ev_in[c].record(s_in)
             s_cmp.wait_event(ev_in[c])
             rc = L.adamw_step(plans[c].handle, groups, ng, None, steps[c:c + 1].data_ptr(),
@@ -479,6 +493,8 @@ def main(argv=None):
     ap.add_argument("--prologue", type=float, default=None, metavar="MAX_NORM",
                     help="run the gradient prologue (non-finite check, norm, clip at "
                          "MAX_NORM) before every step and time both")
+    ap.add_argument("--master", action="store_true",
+                    help="fp32 master weights for the 16-bit params")
     ap.add_argument("--grad-sets", type=int, default=8)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--e2e-chunk", type=int, default=1 << 22)
@@ -494,10 +510,13 @@ def main(argv=None):
         import dataclasses
         wl = dataclasses.replace(wl, param_dtype=args.param_dtype,
                                  name=f"{wl.name}_{args.param_dtype}")
+    if args.master and wl.param_dtype == "f32":
+        raise SystemExit("bench.py: --master needs 16-bit params (--param-dtype bf16 or f16)")
     metric = "AdamW step param-elements/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
     config = {"workload": describe(wl, args.state), "elements": wl.total_numel,
               "tensors": len(wl.tensors), "param_dtype": wl.param_dtype,
               "state": args.state, "groups": len(wl.groups),
+              "master_weights": bool(args.master),
               "l2": "inputs larger than L2 (no flush needed)"
                     if wl.total_numel * BYTES_PER_ELEM[(wl.param_dtype, args.state)] > 4 * 129e6
                     else "inputs smaller than L2"}
@@ -505,7 +524,7 @@ def main(argv=None):
     if args.impl == "reference":
         if rank != 0:
             return 0
-        cb = reference_arm(wl, args.state, args.steps, args.warmup)
+        cb = reference_arm(wl, args.state, args.steps, args.warmup, master=args.master)
         v = cb["value"]
         line = {"impl": "reference", "metric": metric, "value": v, "unit": "param-elements/s",
                 "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
@@ -527,7 +546,8 @@ def main(argv=None):
     res = run_native(args, wl, rank, world, dev)
     if rank != 0:
         return 0
-    cb = None if args.no_cpu_baseline or world > 1 else cpu_baseline(wl, args.state, args.cpu_budget)
+    cb = None if args.no_cpu_baseline or world > 1 else cpu_baseline(wl, args.state, args.cpu_budget,
+                                                                    master=args.master)
     line = {"metric": metric, "value": res["value"], "unit": "param-elements/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": res["ms_per_step"], "higher_is_better": True,

@@ -48,7 +48,7 @@ class adamw_tensor_t(ctypes.Structure):
                 ("m", ctypes.c_void_p), ("v", ctypes.c_void_p),
                 ("m_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
                 ("numel", ctypes.c_int64), ("param_dtype", ctypes.c_int32),
-                ("group", ctypes.c_int32)]
+                ("group", ctypes.c_int32), ("master", ctypes.c_void_p)]
 
 
 class adamw_plan_info_t(ctypes.Structure):
@@ -161,15 +161,18 @@ def adamw_strerror(code: int) -> str:
 
 
 def tensor_desc(param, grad, m, v, m_scale=None, v_scale=None, group: int = 0,
-                numel: Optional[int] = None, param_dtype: Optional[str] = None) -> adamw_tensor_t:
-    """An ``adamw_tensor_t`` from torch tensors (or int addresses + numel/dtype)."""
+                numel: Optional[int] = None, param_dtype: Optional[str] = None,
+                master=None) -> adamw_tensor_t:
+    """An ``adamw_tensor_t`` from torch tensors (or int addresses + numel/dtype);
+    ``master``: optional fp32 master weights of a 16-bit param."""
     if numel is None:
         numel = int(param.numel())
     if param_dtype is None:
         param_dtype = {"torch.float32": "f32", "torch.bfloat16": "bf16",
                        "torch.float16": "f16"}[str(param.dtype)]
     return adamw_tensor_t(_ptr(param), _ptr(grad), _ptr(m), _ptr(v), _ptr(m_scale),
-                          _ptr(v_scale), int(numel), DTYPE_CODES[param_dtype], int(group))
+                          _ptr(v_scale), int(numel), DTYPE_CODES[param_dtype], int(group),
+                          _ptr(master))
 
 
 def adamw_plan_create(tensors: Sequence[adamw_tensor_t], state_kind="f32",

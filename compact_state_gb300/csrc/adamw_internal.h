@@ -73,10 +73,10 @@ struct alignas(16) TensorDesc {
   void* v;
   float* m_scale;
   float* v_scale;
-  int64_t numel;
+  float* master;         // fp32 master weights of a 16-bit param, or null
   int16_t group;
-  uint8_t param_dtype;   // CS_DTYPE_*
-  uint8_t flags;         // kVec | kBulk
+  uint8_t param_dtype;   // CS_DTYPE_* of param and grad
+  uint8_t flags;         // kVec | kBulk | kBulkScale | kMaster
   int32_t n_units;       // work units of this tensor (commit counter target)
 };
 static_assert(sizeof(TensorDesc) == 64, "descriptor must stay 64 bytes");
@@ -84,7 +84,11 @@ enum : uint8_t {
   kVec = 1,    // every buffer aligned to four elements: vector loads
   kBulk = 2,   // every buffer 16-byte aligned: bulk (TMA) copies
   kBulkScale = 4,  // int8 scale arrays 16-byte aligned
+  kMaster = 8,     // theta lives in `master` (fp32); param is its 16-bit copy
 };
+// How a tile reads and writes theta: the param dtype, or an fp32 master with
+// a 16-bit copy (kThetaMasterBF16 / kThetaMasterF16 = dtype + 2).
+enum : int32_t { kThetaMasterBF16 = 3, kThetaMasterF16 = 4 };
 
 // One work unit: `len` elements of tensor `tensor` starting at `start`.
 struct alignas(16) WorkUnit {
@@ -130,11 +134,15 @@ namespace host {
 int elem_bytes(int32_t dtype);
 int state_elem_bytes(int32_t kind);
 int check_tensor(const adamw_tensor_t& t, int32_t state_kind, uint8_t* flags);
+uint8_t access_flags(const adamw_tensor_t& t, int32_t state_kind);
+// The device descriptor of a checked tensor (n_units left 0).
+TensorDesc make_desc(const adamw_tensor_t& t, int32_t state_kind, uint8_t flags);
 int check_group(const adamw_group_t& g);
 }  // namespace host
 
-// Launch one step. Defined in adamw_kernels.cu.
-cudaError_t launch_step(int state_kind, ArgClass cls, const void* args,
+// Launch one step. Defined in adamw_kernels.cu. `master`: some tensor of the
+// launch has fp32 master weights (selects the kernel built with those modes).
+cudaError_t launch_step(int state_kind, ArgClass cls, bool master, const void* args,
                         int grid, cudaStream_t stream);
 // Max resident CTAs per SM of the kernel for (state_kind, cls); also sets the
 // kernel's dynamic shared memory limit.

@@ -81,7 +81,7 @@ int launch_args(const TensorDesc* descs, const WorkUnit* units, uint32_t* commit
                 uint32_t* sched, int32_t n_units, int32_t n_tensors, int state_kind,
                 ArgClass cls, int grid, const adamw_group_t* groups, int32_t n_groups,
                 const uint32_t* present, int32_t* step, const float* inv_scale,
-                const float* found_inf, cudaStream_t stream) {
+                const float* found_inf, bool master, cudaStream_t stream) {
   StepArgs<G, W> a;
   std::memset(&a, 0, sizeof(a));
   a.descs = descs;
@@ -102,7 +102,7 @@ int launch_args(const TensorDesc* descs, const WorkUnit* units, uint32_t* commit
   } else {
     a.all_present = 1;
   }
-  return launch_step(state_kind, cls, &a, std::min(grid, n_units), stream) == cudaSuccess
+  return launch_step(state_kind, cls, master, &a, std::min(grid, n_units), stream) == cudaSuccess
              ? CS_OK
              : CS_ERR_CUDA;
 }
@@ -127,6 +127,7 @@ extern "C" int adamw_step_noalloc(const adamw_tensor_t* tensors, int32_t n_tenso
   std::lock_guard<std::mutex> lock(g_mu);
   // this call's descriptors and work units, in host staging (no allocation)
   int64_t nu = 0;
+  bool any_master = false;
   for (int32_t i = 0; i < n_tensors; ++i) {
     const adamw_tensor_t& t = tensors[i];
     uint8_t flags = 0;
@@ -137,17 +138,8 @@ extern "C" int adamw_step_noalloc(const adamw_tensor_t* tensors, int32_t n_tenso
         t.numel == 0 ? 1 : (t.numel + kDefaultUnitElems - 1) / kDefaultUnitElems;
     if (nu + units > kNaMaxUnits) return CS_ERR_LIMIT;
     TensorDesc& d = g_stage_descs[i];
-    std::memset(&d, 0, sizeof(d));
-    d.param = t.param;
-    d.grad = t.grad;
-    d.m = t.m;
-    d.v = t.v;
-    d.m_scale = state_kind == CS_STATE_INT8 ? t.m_scale : nullptr;
-    d.v_scale = state_kind == CS_STATE_INT8 ? t.v_scale : nullptr;
-    d.numel = t.numel;
-    d.group = static_cast<int16_t>(t.group);
-    d.param_dtype = static_cast<uint8_t>(t.param_dtype);
-    d.flags = flags;
+    d = host::make_desc(t, state_kind, flags);
+    any_master = any_master || t.master != nullptr;
     d.n_units = static_cast<int32_t>(units);
     for (int64_t k = 0; k < units; ++k) {
       WorkUnit& w = g_stage_units[nu + k];
@@ -188,9 +180,10 @@ extern "C" int adamw_step_noalloc(const adamw_tensor_t* tensors, int32_t n_tenso
     return launch_args<kSmallGroups, kSmallWords>(
         d_descs, d_units, d_commit, d_sched, n_units, n_tensors, state_kind, kClassSmall,
         nd->grid[state_kind][kClassSmall], groups, n_groups, grad_present, step, inv_scale,
-        found_inf, s);
+        found_inf, any_master, s);
   return launch_args<kMidGroups, kMidWords>(d_descs, d_units, d_commit, d_sched, n_units,
                                             n_tensors, state_kind, kClassMid,
                                             nd->grid[state_kind][kClassMid], groups, n_groups,
-                                            grad_present, step, inv_scale, found_inf, s);
+                                            grad_present, step, inv_scale, found_inf,
+                                            any_master, s);
 }

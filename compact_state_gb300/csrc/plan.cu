@@ -20,6 +20,7 @@ struct adamw_plan {
   int32_t unit_elems = 0;
   int32_t max_group = 0;
   int32_t sm_count = 0;
+  bool any_master = false;         // some tensor has fp32 master weights
   int64_t n_units = 0;
   int64_t total_numel = 0;
   int64_t device_bytes = 0;
@@ -35,6 +36,7 @@ struct adamw_plan {
   uint64_t wait_ns = cs::kDefaultWaitNs;
   uint32_t debug = 0;
   std::vector<TensorDesc> h_descs;
+  std::vector<int64_t> h_numel;
   TensorDesc* h_staging = nullptr;   // pinned, for adamw_plan_set_grads
   cudaEvent_t staging_done = nullptr;
   bool staging_pending = false;
@@ -63,35 +65,66 @@ int state_elem_bytes(int32_t kind) {
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
-uint8_t access_flags(const void* param, const void* grad, const void* m, const void* v,
-                     const float* ms, const float* vs, int pb, int sb, int32_t state_kind) {
+// Vector access needs every buffer aligned to four of its elements, bulk
+// copies 16-byte alignment of everything they load (theta comes from the
+// master when there is one; param is then only stored, four at a time).
+uint8_t access_flags(const adamw_tensor_t& t, int32_t state_kind) {
+  const int pb = elem_bytes(t.param_dtype);
+  const int sb = state_elem_bytes(state_kind);
+  const bool vec_core = aligned(t.param, 4 * pb) && aligned(t.grad, 4 * pb) &&
+                        aligned(t.m, 4 * sb) && aligned(t.v, 4 * sb);
+  const bool bulk_core = aligned(t.grad, 16) && aligned(t.m, 16) && aligned(t.v, 16);
   uint8_t f = 0;
-  if (aligned(param, 4 * pb) && aligned(grad, 4 * pb) && aligned(m, 4 * sb) && aligned(v, 4 * sb))
-    f |= cs::kVec;
-  if (aligned(param, 16) && aligned(grad, 16) && aligned(m, 16) && aligned(v, 16)) f |= cs::kBulk;
-  if (state_kind == CS_STATE_INT8 && aligned(ms, 16) && aligned(vs, 16)) f |= cs::kBulkScale;
+  if (t.master) {
+    f |= cs::kMaster;
+    if (vec_core && aligned(t.master, 16)) f |= cs::kVec;
+    if (bulk_core && aligned(t.master, 16) && aligned(t.param, 4 * pb)) f |= cs::kBulk;
+  } else {
+    if (vec_core) f |= cs::kVec;
+    if (bulk_core && aligned(t.param, 16)) f |= cs::kBulk;
+  }
+  if (state_kind == CS_STATE_INT8 && aligned(t.m_scale, 16) && aligned(t.v_scale, 16))
+    f |= cs::kBulkScale;
   return f;
 }
 
-// Validates one tensor; sets *flags to its access flags (vector, bulk).
-int check_tensor(const adamw_tensor_t& t, int32_t state_kind, uint8_t* vec_ok) {
+// Validates one tensor; sets *flags to its access flags.
+int check_tensor(const adamw_tensor_t& t, int32_t state_kind, uint8_t* flags) {
   if (t.numel < 0 || t.group < 0) return CS_ERR_INVALID_ARGUMENT;
   const int pb = elem_bytes(t.param_dtype);
   if (pb == 0) return CS_ERR_UNSUPPORTED;
   if (t.group >= CS_MAX_GROUPS) return CS_ERR_LIMIT;
-  *vec_ok = 0;
+  if (t.master && t.param_dtype == CS_DTYPE_F32) return CS_ERR_INVALID_ARGUMENT;
+  *flags = t.master ? cs::kMaster : 0;
   if (t.numel == 0) return CS_OK;
   if (t.numel > (int64_t(1) << 40)) return CS_ERR_LIMIT;
   const int sb = state_elem_bytes(state_kind);
   if (!t.param || !t.grad || !t.m || !t.v) return CS_ERR_INVALID_ARGUMENT;
   if (!aligned(t.param, pb) || !aligned(t.grad, pb) || !aligned(t.m, sb) || !aligned(t.v, sb))
     return CS_ERR_MISALIGNED;
+  if (t.master && !aligned(t.master, 4)) return CS_ERR_MISALIGNED;
   if (state_kind == CS_STATE_INT8) {
     if (!t.m_scale || !t.v_scale) return CS_ERR_INVALID_ARGUMENT;
     if (!aligned(t.m_scale, 4) || !aligned(t.v_scale, 4)) return CS_ERR_MISALIGNED;
   }
-  *vec_ok = access_flags(t.param, t.grad, t.m, t.v, t.m_scale, t.v_scale, pb, sb, state_kind);
+  *flags = access_flags(t, state_kind);
   return CS_OK;
+}
+
+TensorDesc make_desc(const adamw_tensor_t& t, int32_t state_kind, uint8_t flags) {
+  TensorDesc d;
+  std::memset(&d, 0, sizeof(d));
+  d.param = t.param;
+  d.grad = t.grad;
+  d.m = t.m;
+  d.v = t.v;
+  d.m_scale = state_kind == CS_STATE_INT8 ? t.m_scale : nullptr;
+  d.v_scale = state_kind == CS_STATE_INT8 ? t.v_scale : nullptr;
+  d.master = t.master;
+  d.group = static_cast<int16_t>(t.group);
+  d.param_dtype = static_cast<uint8_t>(t.param_dtype);
+  d.flags = flags;
+  return d;
 }
 
 int check_unit_elems(int32_t unit_elems, int32_t* out) {
@@ -180,7 +213,8 @@ int launch_class(adamw_plan* p, cs::ArgClass cls, const adamw_group_t* groups,
   } else {
     a.all_present = 1;
   }
-  const cudaError_t e = cs::launch_step(p->state_kind, cls, &a, p->grid[cls], stream);
+  const cudaError_t e =
+      cs::launch_step(p->state_kind, cls, p->any_master, &a, p->grid[cls], stream);
   return e == cudaSuccess ? CS_OK : CS_ERR_CUDA;
 }
 
@@ -304,18 +338,8 @@ int adamw_plan_create(const adamw_tensor_t* tensors, int32_t n_tensors, int32_t 
       uint8_t vec = 0;
       rc = check_tensor(t, state_kind, &vec);
       if (rc) { delete p; return rc; }
-      TensorDesc& d = p->h_descs[i];
-      std::memset(&d, 0, sizeof(d));
-      d.param = t.param;
-      d.grad = t.grad;
-      d.m = t.m;
-      d.v = t.v;
-      d.m_scale = state_kind == CS_STATE_INT8 ? t.m_scale : nullptr;
-      d.v_scale = state_kind == CS_STATE_INT8 ? t.v_scale : nullptr;
-      d.numel = t.numel;
-      d.group = static_cast<int16_t>(t.group);
-      d.param_dtype = static_cast<uint8_t>(t.param_dtype);
-      d.flags = vec;
+      p->h_descs[i] = make_desc(t, state_kind, vec);
+      p->any_master = p->any_master || t.master != nullptr;
       numels[i] = t.numel;
       p->total_numel += t.numel;
       p->max_group = std::max(p->max_group, t.group);
@@ -323,6 +347,7 @@ int adamw_plan_create(const adamw_tensor_t* tensors, int32_t n_tensors, int32_t 
     std::vector<WorkUnit> units;
     std::vector<int32_t> per;
     build_units(numels.data(), n_tensors, ue, &units, &per);
+    p->h_numel = numels;
     if (units.size() >= (size_t(1) << 31) - (size_t(1) << 20)) { delete p; return CS_ERR_LIMIT; }
     for (int32_t i = 0; i < n_tensors; ++i) p->h_descs[i].n_units = per[i];
     p->n_units = static_cast<int64_t>(units.size());
@@ -455,7 +480,7 @@ int adamw_plan_set_grads(adamw_plan_t* p, const void* const* grads, struct CUstr
   // validate first: nothing changes on error
   for (int32_t i = 0; i < p->n_tensors; ++i) {
     const TensorDesc& d = p->h_descs[i];
-    if (d.numel == 0) continue;
+    if (p->h_numel[i] == 0) continue;
     const int pb = elem_bytes(d.param_dtype);
     if (!grads[i]) return CS_ERR_INVALID_ARGUMENT;
     if (!aligned(grads[i], pb)) return CS_ERR_MISALIGNED;
@@ -473,12 +498,18 @@ int adamw_plan_set_grads(adamw_plan_t* p, const void* const* grads, struct CUstr
   if (p->staging_pending && cudaEventSynchronize(p->staging_done) != cudaSuccess) return CS_ERR_CUDA;
   for (int32_t i = 0; i < p->n_tensors; ++i) {
     TensorDesc& d = p->h_descs[i];
-    if (d.numel == 0) continue;
-    const int pb = elem_bytes(d.param_dtype);
-    const int sb = state_elem_bytes(p->state_kind);
+    if (p->h_numel[i] == 0) continue;
     d.grad = grads[i];
-    d.flags = access_flags(d.param, d.grad, d.m, d.v, d.m_scale, d.v_scale, pb, sb,
-                           p->state_kind);
+    adamw_tensor_t t{};
+    t.param = d.param;
+    t.grad = d.grad;
+    t.m = d.m;
+    t.v = d.v;
+    t.m_scale = d.m_scale;
+    t.v_scale = d.v_scale;
+    t.master = d.master;
+    t.param_dtype = d.param_dtype;
+    d.flags = access_flags(t, p->state_kind);
   }
   std::memcpy(p->h_staging, p->h_descs.data(), bytes);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

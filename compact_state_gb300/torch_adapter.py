@@ -21,11 +21,14 @@ class AdamWState:
 
     params, grads: same-length lists of CUDA tensors (grads same dtype/numel).
     group_of: per-tensor group index (default 0).
+    master: keep fp32 master weights for the 16-bit params (initialised to
+    their exact fp32 values); the step then updates the master and writes
+    each 16-bit param as its rounding.
     """
 
     def __init__(self, params: Sequence[torch.Tensor], grads: Sequence[torch.Tensor],
                  state_kind: str = "f32", group_of: Optional[Sequence[int]] = None,
-                 unit_elems: int = 0):
+                 unit_elems: int = 0, master: bool = False):
         if len(params) != len(grads):
             raise ValueError("params and grads differ in length")
         self.params = list(params)
@@ -39,6 +42,7 @@ class AdamWState:
         self.v: List[torch.Tensor] = []
         self.m_scale: List[Optional[torch.Tensor]] = []
         self.v_scale: List[Optional[torch.Tensor]] = []
+        self.master: List[Optional[torch.Tensor]] = []
         descs = []
         for p, g, grp in zip(self.params, self.grads, self.group_of):
             if p.numel() != g.numel() or p.dtype != g.dtype:
@@ -56,7 +60,11 @@ class AdamWState:
             self.v.append(v)
             self.m_scale.append(ms)
             self.v_scale.append(vs)
-            descs.append(tensor_desc(p, g, m, v, ms, vs, group=grp))
+            mw = None
+            if master and p.dtype != torch.float32:
+                mw = p.detach().reshape(-1).to(torch.float32)
+            self.master.append(mw)
+            descs.append(tensor_desc(p, g, m, v, ms, vs, group=grp, master=mw))
         self.step = torch.zeros(max(n, 1), dtype=torch.int32, device=dev)
         self.plan: Plan = adamw_plan_create(descs, state_kind, unit_elems)
 

@@ -103,6 +103,16 @@ typedef struct adamw_tensor_t {
                             step count still advances when it has a grad)    */
     int32_t     param_dtype;  /* CS_DTYPE_*; grad has the same dtype         */
     int32_t     group;        /* index into the per-step group table         */
+    float      *master;  /* device, optional fp32 master weights (numel
+                            values) of a CS_DTYPE_BF16 / CS_DTYPE_F16 param,
+                            or NULL. With a master the step reads the master,
+                            not param; it stores the new value to the master
+                            and its round-to-nearest-even to param, in the
+                            same pass (the Apex fused-optimizers guide,
+                            FusedAdam master_weights, sections 4.2 and 4.3).
+                            The caller initialises it, usually to param's
+                            exact fp32 value. A master on an fp32 param is
+                            CS_ERR_INVALID_ARGUMENT.                       */
 } adamw_tensor_t;
 
 /* Moments start at zero: the caller zero-fills m and v (and, for int8, the

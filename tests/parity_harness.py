@@ -13,6 +13,11 @@ Two modes, both on the same seeded inputs (``workloads``):
                scales <= 1e-6 relative, fp32 values by the fp32 rule,
                bf16/fp16 params <= 1 ulp of their format, step counts exact.
 
+With fp32 master weights (``master=True``, 16-bit params) the master is
+compared by the fp32 rule, and the 16-bit param must equal torch's rounding of
+the GPU's own master bit for bit, besides the 16-bit param bar against the
+oracle.
+
 Positions are either whole tensors or a seeded sample (whole 256-element blocks
 for int8 state), so full-size workloads can be checked element by element.
 Steps whose found_inf flag is set and tensors without a gradient are checked
@@ -144,7 +149,7 @@ class Harness:
     def __init__(self, wl: workloads.Workload, state_kind: str, unit_elems: int = 0,
                  sample: Optional[int] = None, grad_device: str = "cpu",
                  param_device_init: str = "cpu", misalign: bool = False,
-                 device: str = "cuda", seed: int = 0):
+                 device: str = "cuda", seed: int = 0, master: bool = False):
         from compact_state_gb300.torch_adapter import AdamWState
         self.wl = wl
         self.kind = state_kind
@@ -169,8 +174,9 @@ class Harness:
             g.zero_()
             self.params.append(p)
             self.grads.append(g)
+        self.master = master
         self.state = AdamWState(self.params, self.grads, state_kind,
-                                [t.group for t in wl.tensors], unit_elems)
+                                [t.group for t in wl.tensors], unit_elems, master=master)
         if misalign:
             # moments of the misaligned case start one element into a buffer too
             self._misalign_state(pdt)
@@ -198,7 +204,8 @@ class Harness:
         self.ostates: List[TensorState] = []
         for i, spec in enumerate(wl.tensors):
             th = torch_to_f64(self.params[i].view(-1)[self.tidx[i]])
-            self.ostates.append(new_state(th, self.fmt, state_kind, group=spec.group))
+            self.ostates.append(new_state(th, self.fmt, state_kind, group=spec.group,
+                                          master=master))
         self.gpu_groups = self._gpu_groups()
         self.inv_scale_t = torch.tensor([wl.inv_scale], dtype=torch.float32, device=self.dev)
         self.found_inf_t = torch.zeros(1, dtype=torch.float32, device=self.dev)
@@ -216,8 +223,14 @@ class Harness:
             bv = torch.zeros(spec.numel + 1, dtype=sdt, device=self.dev)
             self._storage += [bm, bv]
             st.m[i], st.v[i] = bm[1:], bv[1:]
+            if st.master[i] is not None:
+                bw = torch.empty(spec.numel + 1, dtype=torch.float32, device=self.dev)
+                bw[1:].copy_(st.master[i])
+                self._storage.append(bw)
+                st.master[i] = bw[1:]
             descs.append(tensor_desc(self.params[i], self.grads[i], st.m[i], st.v[i],
-                                     st.m_scale[i], st.v_scale[i], group=spec.group))
+                                     st.m_scale[i], st.v_scale[i], group=spec.group,
+                                     master=st.master[i]))
         st.plan = adamw_plan_create(descs, self.kind, 0)
 
     def _gpu_groups(self):
@@ -254,6 +267,8 @@ class Harness:
         for i, o in enumerate(self.ostates):
             ix = self.tidx[i]
             self.params[i].view(-1)[ix] = f64_to_torch(o.theta, pdt, self.dev)
+            if o.master is not None:
+                st.master[i][ix] = f64_to_torch(o.master, torch.float32, self.dev)
             if self.kind == "int8":
                 st.m[i][ix] = torch.from_numpy(o.m).to(self.dev)
                 st.v[i][ix] = torch.from_numpy(o.v).to(self.dev)
@@ -292,9 +307,9 @@ class Harness:
 
     def snapshot(self):
         st = self.state
+        c = lambda x: None if x is None else x.clone()
         return [(self.params[i].clone(), st.m[i].clone(), st.v[i].clone(),
-                 None if st.m_scale[i] is None else st.m_scale[i].clone(),
-                 None if st.v_scale[i] is None else st.v_scale[i].clone())
+                 c(st.m_scale[i]), c(st.v_scale[i]), c(st.master[i]))
                 for i in range(len(self.params))], st.step.clone()
 
     def assert_unchanged(self, snap, tensors):
@@ -302,8 +317,10 @@ class Harness:
         st = self.state
         cur_steps = st.step
         for i in tensors:
-            p, m, v, ms, vs = bufs[i]
+            p, m, v, ms, vs, mw = bufs[i]
             assert _bits_equal(p, self.params[i]), f"param {i} changed"
+            if mw is not None:
+                assert _bits_equal(mw, st.master[i]), f"master {i} changed"
             assert _bits_equal(m, st.m[i]), f"m {i} changed"
             assert _bits_equal(v, st.v[i]), f"v {i} changed"
             if ms is not None:
@@ -357,6 +374,15 @@ class Harness:
         mv = {"m": ([], []), "v": ([], [])}
         for i, o in enumerate(self.ostates):
             th, m, v, ms, vs = self._gpu_state(i)
+            if o.master is not None:
+                # the master by the fp32 rule; the 16-bit param is exactly the
+                # rounding of the GPU's own master
+                mw = self.state.master[i][self.tidx[i]]
+                th_all.append(torch_to_f64(mw))
+                thr_all.append(o.master)
+                cast = torch_to_f64(mw.to(workloads.torch_dtype(self.fmt)))
+                upd("copy_mismatch", int(np.sum(~((cast == th) | (np.isnan(cast) &
+                                                                   np.isnan(th))))))
             if self.fmt == "f32":
                 th_all.append(th)
                 thr_all.append(o.theta)
@@ -420,10 +446,10 @@ def _bits_equal(a: torch.Tensor, b: torch.Tensor) -> bool:
 def check_bars(res: Result, kind: str, fmt: str, forced: bool) -> None:
     """Assert the tolerances for the mode that ran."""
     w = res.forced if forced else res.free
-    if fmt == "f32":
-        assert w.get("theta_excess", 0) <= 1.0, w
-    else:
+    assert w.get("theta_excess", 0) <= 1.0, w       # fp32 params, or fp32 masters
+    if fmt != "f32":
         assert w.get("theta16_excess", 0) <= 1.0, w
+    assert w.get("copy_mismatch", 0) == 0, w
     if kind == "f32":
         assert w.get("m_excess", 0) <= 1.0 and w.get("v_excess", 0) <= 1.0, w
     elif kind == "bf16":

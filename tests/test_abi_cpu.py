@@ -133,6 +133,8 @@ def _desc(cs, **kw):
     (dict(m=0x30002), "f32", -3),
     (dict(m_scale=0), "int8", -1),
     (dict(v_scale=0x60002), "int8", -3),
+    (dict(master=0x70000), "f32", -1),        # a master needs a 16-bit param
+    (dict(master=0x70002, param_dtype=1), "f32", -3),   # master not 4-byte aligned
 ])
 def test_plan_create_rejects_invalid_tensors(cs, kw, state, code):
     arr = (cs.adamw_tensor_t * 2)(_desc(cs), _desc(cs, **kw))
@@ -169,3 +171,9 @@ def test_valid_plan_without_gpu_reports_cuda_error(cs):
     out = ctypes.c_void_p()
     assert cs.lib().adamw_plan_create(arr, 1, 0, 0, ctypes.byref(out)) == -5
     assert out.value is None
+
+
+def test_tensor_struct_layout_matches_header(cs):
+    # the C struct: six pointers, int64 numel, two int32, then the master pointer
+    assert ctypes.sizeof(cs.adamw_tensor_t) == 72
+    assert cs.adamw_tensor_t.master.offset == 64
