@@ -13,6 +13,10 @@ Precision, xuujii.github.io ai-infra-kb M041):
 * ``int8_block`` -- the teaching signed block codec of section 05
                     (scale = max|x|/127, q = round(x/scale), x ~ q*scale,
                     all-zero blocks handled separately).
+* ``dynamic8``   -- the non-linear 8-bit codebook variant of section 05 (the
+                    published dynamic tree quantization; signed for m,
+                    unsigned for v), one fp32 absmax per 256-element block.
+                    ``int8_block`` also holds the unsigned linear variant for v.
 * ``adamw``      -- the AdamW update of section 02 in the page's own order, the
                     three-separate-loops form of section 04, and the step/skip
                     contract of sections 02, 03 and 06 (grad=None skips a tensor,
@@ -35,7 +39,13 @@ What pins each function (tests marked ``not gpu``):
                             unscale-by-power-of-two identity, and equality with
                             the three-loop form.
 * ``state_bytes``           the benchmark page's 185.501 / 92.751 / 47.101 MB.
+* ``int8_block`` (unsigned) the bound, max -> 255, exact multiples, brute-force
+                            nearest code, half the signed codec's error.
+* ``dynamic8``              the table's structure from its bit layout (decade
+                            tops against fp32(10^-E), equal in-decade steps),
+                            brute-force nearest-code search, the per-decade
+                            error bound, small values kept next to an outlier.
 """
-from . import formats, int8_block, adamw, state_bytes  # noqa: F401
+from . import formats, int8_block, dynamic8, adamw, state_bytes  # noqa: F401
 from .adamw import (TensorState, adamw_update, oracle_step,  # noqa: F401
                     oracle_step_three_loops, new_state)

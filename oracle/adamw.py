@@ -49,8 +49,21 @@ from typing import List, Optional, Sequence
 
 import numpy as np
 
-from . import int8_block
+from . import dynamic8, int8_block
 from .formats import round_to
+
+# 8-bit state kinds: (encode, decode, code dtype) for m, then for v.
+#   "int8"   -- the signed linear block codec for both moments (section 05);
+#   "int8uv" -- signed linear m, unsigned linear v (scale max/255);
+#   "dyn8"   -- the dynamic-exponent codebook, signed for m, unsigned for v.
+CODECS = {
+    "int8": ((int8_block.encode, int8_block.decode, np.int8),
+             (int8_block.encode, int8_block.decode, np.int8)),
+    "int8uv": ((int8_block.encode, int8_block.decode, np.int8),
+               (int8_block.encode_unsigned, int8_block.decode_unsigned, np.uint8)),
+    "dyn8": ((dynamic8.encode_signed, dynamic8.decode_signed, np.uint8),
+             (dynamic8.encode_unsigned, dynamic8.decode_unsigned, np.uint8)),
+}
 
 
 def adamw_update(theta, g, m, v, t, lr, beta1, beta2, eps, weight_decay):
@@ -73,8 +86,8 @@ class TensorState:
 
     ``theta`` holds float64 values representable in ``param_fmt``. For state
     kinds "f32"/"bf16", ``m``/``v`` hold float64 values representable in that
-    format; for "int8" they hold int8 codes and ``m_scale``/``v_scale`` fp32
-    per-block scales.
+    format; for the 8-bit kinds (``CODECS``) they hold 8-bit codes and
+    ``m_scale``/``v_scale`` fp32 per-block scales.
     """
     theta: np.ndarray
     param_fmt: str
@@ -99,9 +112,9 @@ class TensorState:
 
     # -- decode / encode ---------------------------------------------------
     def moments(self):
-        if self.state_kind == "int8":
-            return (int8_block.decode(self.m, self.m_scale),
-                    int8_block.decode(self.v, self.v_scale))
+        if self.state_kind in CODECS:
+            (_, dec_m, _), (_, dec_v, _) = CODECS[self.state_kind]
+            return dec_m(self.m, self.m_scale), dec_v(self.v, self.v_scale)
         return (np.asarray(self.m, dtype=np.float64),
                 np.asarray(self.v, dtype=np.float64))
 
@@ -111,9 +124,10 @@ class TensorState:
         else:
             self.master = round_to(theta, "f32")
             self.theta = round_to(self.master, self.param_fmt)
-        if self.state_kind == "int8":
-            self.m, self.m_scale = int8_block.encode(m)
-            self.v, self.v_scale = int8_block.encode(v)
+        if self.state_kind in CODECS:
+            (enc_m, _, _), (enc_v, _, _) = CODECS[self.state_kind]
+            self.m, self.m_scale = enc_m(m)
+            self.v, self.v_scale = enc_v(v)
         else:
             self.m = round_to(m, self.state_kind)
             self.v = round_to(v, self.state_kind)
@@ -126,10 +140,11 @@ def new_state(theta, param_fmt: str, state_kind: str, group: int = 0,
     theta = round_to(np.asarray(theta, dtype=np.float64).reshape(-1), param_fmt)
     n = theta.size
     mw = np.array(theta, copy=True) if master else None
-    if state_kind == "int8":
+    if state_kind in CODECS:
         nb = int8_block.n_blocks(n)
-        return TensorState(theta, param_fmt, state_kind, np.zeros(n, np.int8),
-                           np.zeros(n, np.int8), np.zeros(nb, np.float32),
+        (_, _, dm), (_, _, dv) = CODECS[state_kind]
+        return TensorState(theta, param_fmt, state_kind, np.zeros(n, dm),
+                           np.zeros(n, dv), np.zeros(nb, np.float32),
                            np.zeros(nb, np.float32), step, group, mw)
     return TensorState(theta, param_fmt, state_kind, np.zeros(n), np.zeros(n),
                        None, None, step, group, mw)

@@ -11,12 +11,17 @@ Layout counted here (one step counter of 4 bytes per tensor):
 * "f32":  two fp32 moments              -> 8 bytes per element
 * "bf16": two bf16 moments              -> 4 bytes per element
 * "int8": two int8 codes + two fp32 scales per 256-element block of each tensor
+* "int8uv", "dyn8": the same bytes (other codecs, section 05 variants)
+
+Selective precision (section 05 cites bitsandbytes' selective high-precision
+settings): with ``min_8bit_size``, tensors smaller than it keep fp32 moments.
 """
 from __future__ import annotations
 
 from typing import Iterable
 
-BYTES_PER_ELEM = {"f32": 8, "bf16": 4, "int8": 2}
+BYTES_PER_ELEM = {"f32": 8, "bf16": 4, "int8": 2, "int8uv": 2, "dyn8": 2}
+EIGHT_BIT = ("int8", "int8uv", "dyn8")
 STEP_BYTES = 4
 BLOCK = 256
 SCALE_BYTES = 4
@@ -24,12 +29,20 @@ SCALE_BYTES = 4
 
 def tensor_state_bytes(n: int, state_kind: str, with_step: bool = True) -> int:
     b = BYTES_PER_ELEM[state_kind] * int(n)
-    if state_kind == "int8":
+    if state_kind in EIGHT_BIT:
         b += 2 * SCALE_BYTES * (-(-int(n) // BLOCK))
     if with_step:
         b += STEP_BYTES
     return b
 
 
-def state_bytes(numels: Iterable[int], state_kind: str, with_step: bool = True) -> int:
-    return sum(tensor_state_bytes(n, state_kind, with_step) for n in numels)
+def kind_for(n: int, state_kind: str, min_8bit_size: int = 0) -> str:
+    """Selective precision: an 8-bit plan keeps fp32 moments for tensors with
+    fewer than ``min_8bit_size`` elements."""
+    return "f32" if state_kind in EIGHT_BIT and int(n) < min_8bit_size else state_kind
+
+
+def state_bytes(numels: Iterable[int], state_kind: str, with_step: bool = True,
+                min_8bit_size: int = 0) -> int:
+    return sum(tensor_state_bytes(n, kind_for(n, state_kind, min_8bit_size), with_step)
+               for n in numels)

@@ -167,7 +167,7 @@ def test_grad_none_untouched_zero_grad_updates():
     assert not np.array_equal(b.theta, b0.theta)
 
 
-@pytest.mark.parametrize("state_kind", ["f32", "bf16", "int8"])
+@pytest.mark.parametrize("state_kind", ["f32", "bf16", "int8", "int8uv", "dyn8"])
 def test_found_inf_leaves_everything_untouched(state_kind):
     rng = np.random.default_rng(6)
     grp = [dict(lr=1e-2, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1)]
@@ -183,7 +183,7 @@ def test_found_inf_leaves_everything_untouched(state_kind):
             assert (x is None and y is None) or x.tobytes() == y.tobytes()
 
 
-@pytest.mark.parametrize("state_kind", ["f32", "bf16", "int8"])
+@pytest.mark.parametrize("state_kind", ["f32", "bf16", "int8", "int8uv", "dyn8"])
 def test_power_of_two_unscale_is_exact(state_kind):
     rng = np.random.default_rng(8)
     grp = [dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01)]
@@ -198,7 +198,7 @@ def test_power_of_two_unscale_is_exact(state_kind):
         assert getattr(a[0], f).tobytes() == getattr(b[0], f).tobytes()
 
 
-@pytest.mark.parametrize("state_kind", ["f32", "bf16", "int8"])
+@pytest.mark.parametrize("state_kind", ["f32", "bf16", "int8", "int8uv", "dyn8"])
 def test_three_loops_equal_fused(state_kind):
     rng = np.random.default_rng(9)
     groups = [dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01),

@@ -60,3 +60,16 @@ def test_seeded_fills_are_deterministic():
     flat = g.view(-1)
     for b in zb:
         assert torch.all(flat[b * 256:(b + 1) * 256] == 0)
+
+
+def test_selective_fp32_for_small_tensors():
+    # 100 and 4095 elements stay fp32 (8 B each), 4096 and 5000 are coded
+    # (2 B each plus two fp32 scales per 256-block), plus a 4 B step per tensor
+    from oracle.state_bytes import kind_for
+    sb = state_bytes.state_bytes
+    numels = [100, 5000, 4095, 4096]
+    want = (8 * (100 + 4095) + 2 * (5000 + 4096) + 2 * 4 * (20 + 16) + 4 * 4)
+    for kind in ("int8", "int8uv", "dyn8"):
+        assert sb(numels, kind, min_8bit_size=4096) == want
+        assert kind_for(4095, kind, 4096) == "f32" and kind_for(4096, kind, 4096) == kind
+    assert kind_for(10, "bf16", 4096) == "bf16"       # only 8-bit kinds are affected
