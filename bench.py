@@ -40,6 +40,9 @@ BYTES_PER_ELEM = {  # (param dtype, state kind) -> read + write bytes per elemen
     ("f32", "bf16"): 20, ("bf16", "bf16"): 14, ("f16", "bf16"): 14,
     ("f32", "int8"): 16.0625, ("bf16", "int8"): 10.0625, ("f16", "int8"): 10.0625,
 }
+for _p in ("f32", "bf16", "f16"):       # the other 8-bit codecs move the same bytes
+    for _k in ("int8uv", "dyn8"):
+        BYTES_PER_ELEM[(_p, _k)] = BYTES_PER_ELEM[(_p, "int8")]
 FALLBACK_HBM_GBS = 6800.0
 
 
@@ -49,7 +52,7 @@ def bytes_per_elem(param_dtype: str, state: str, master: bool = False) -> float:
     written to both (4 + 2 B instead of 2): 6 B more."""
     return BYTES_PER_ELEM[(param_dtype, state)] + (6 if master else 0)
 KERNEL_SRCS = [os.path.join(ROOT, "compact_state_gb300", "csrc", f)
-               for f in ("adamw_kernels.cu", "adamw_internal.h")]
+               for f in ("step_kernel.cuh", "adamw_internal.h")]
 
 
 def kernel_hash() -> str:
@@ -224,7 +227,7 @@ def reference_arm(wl, state: str, steps: int, warmup: int, n: int = 1 << 18,
 
 
 # ------------------------------------------------------------------ GPU arm
-def alloc_state(wl, state, dev, master=False):
+def alloc_state(wl, state, dev, master=False, min_8bit_size=0):
     import torch
     import workloads
     from compact_state_gb300.torch_adapter import AdamWState
@@ -235,7 +238,8 @@ def alloc_state(wl, state, dev, master=False):
         p.copy_(workloads.init_param(wl, i, device=dev).reshape(-1))
         params.append(p)
     grads = [torch.empty_like(p) for p in params]
-    st = AdamWState(params, grads, state, [t.group for t in wl.tensors], master=master)
+    st = AdamWState(params, grads, state, [t.group for t in wl.tensors], master=master,
+                    min_8bit_size=min_8bit_size)
     return st
 
 
@@ -260,7 +264,7 @@ def run_native(args, wl, rank, world, dev):
     import compact_state_gb300 as cs
     from compact_state_gb300 import tensor_desc
     state = args.state
-    st = alloc_state(wl, state, dev, args.master)
+    st = alloc_state(wl, state, dev, args.master, args.min_8bit_size)
     plan_info = cs.adamw_plan_info(st.plan)
     # grad buffers: fresh seeded grads per step, cycling through a pool
     per_set = sum(g.numel() * g.element_size() for g in st.grads)
@@ -270,9 +274,10 @@ def run_native(args, wl, rank, world, dev):
     # one plan per grad set (descriptors hold grad pointers)
     plans = [st.plan]
     for gs in sets[1:]:
-        descs = [tensor_desc(p, g, m, v, ms, vs, group=t.group, master=mw)
-                 for p, g, m, v, ms, vs, mw, t in zip(st.params, gs, st.m, st.v, st.m_scale,
-                                                      st.v_scale, st.master, wl.tensors)]
+        descs = [tensor_desc(p, g, m, v, ms, vs, group=t.group, master=mw, flags=int(f32))
+                 for p, g, m, v, ms, vs, mw, f32, t in zip(
+                     st.params, gs, st.m, st.v, st.m_scale, st.v_scale, st.master,
+                     st.fp32_state, wl.tensors)]
         plans.append(cs.adamw_plan_create(descs, state, 0))
     groups = cs.groups_array([dict(lr=g.lr, beta1=g.beta1, beta2=g.beta2, eps=g.eps,
                                    weight_decay=g.weight_decay) for g in wl.groups])
@@ -331,14 +336,17 @@ def run_native(args, wl, rank, world, dev):
     elems = wl.total_numel
     value = world * elems * K / (max_ms / 1e3)
     avg_kernel_ms = sum(per) / len(per)
-    bpe = bytes_per_elem(wl.param_dtype, state, args.master)
+    # per tensor: tensors an 8-bit plan keeps in fp32 move fp32-state bytes
+    bpe = sum(t.numel * bytes_per_elem(wl.param_dtype, "f32" if f32 else state, args.master)
+              for t, f32 in zip(wl.tensors, st.fp32_state)) / max(elems, 1)
     if args.prologue is not None:
         bpe += 4 if wl.param_dtype == "f32" else 2     # the prologue reads the grads once more
     alg_bytes = elems * bpe
     peak, peak_src = hbm_peak()
     achieved = alg_bytes / (avg_kernel_ms / 1e3) / 1e9
     key = (args.workload + (f"_{args.param_dtype}" if args.param_dtype else "")
-           + ("_master" if args.master else ""))
+           + ("_master" if args.master else "")
+           + (f"_min8bit{args.min_8bit_size}" if args.min_8bit_size else ""))
     traffic = committed_traffic(key, state)
     result = dict(
         value=value, ms_per_step=max_ms / K, kernel_ms_avg=avg_kernel_ms,
@@ -384,7 +392,7 @@ def run_e2e(args, wl, st, groups, ng, dev, world):
     for (i, dv) in chunks:
         plans.append(cs.adamw_plan_create(
             [tensor_desc(dv[0], dv[1], dv[2], dv[3], dv[4], dv[5], group=wl.tensors[i].group,
-                         master=dv[6])], args.state, 0))
+                         master=dv[6], flags=int(st.fp32_state[i]))], args.state, 0))
     steps = torch.zeros(len(chunks), dtype=torch.int32, device=dev)
     inv = torch.tensor([wl.inv_scale], dtype=torch.float32, device=dev)
     # in: what the step reads (theta from the master when there is one); out:
@@ -486,7 +494,9 @@ def main(argv=None):
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="few_large",
                     choices=["few_large", "llama3_8b", "many_small", "lora", "tiny"])
-    ap.add_argument("--state", default="f32", choices=["f32", "bf16", "int8"])
+    ap.add_argument("--state", default="f32", choices=["f32", "bf16", "int8", "int8uv", "dyn8"])
+    ap.add_argument("--min-8bit-size", type=int, default=0,
+                    help="with an 8-bit state, tensors below this size keep fp32 moments")
     ap.add_argument("--param-dtype", default=None, choices=["f32", "bf16", "f16"],
                     help="override the workload's param/grad dtype")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
@@ -517,6 +527,7 @@ def main(argv=None):
               "tensors": len(wl.tensors), "param_dtype": wl.param_dtype,
               "state": args.state, "groups": len(wl.groups),
               "master_weights": bool(args.master),
+              "min_8bit_size": args.min_8bit_size,
               "l2": "inputs larger than L2 (no flush needed)"
                     if wl.total_numel * BYTES_PER_ELEM[(wl.param_dtype, args.state)] > 4 * 129e6
                     else "inputs smaller than L2"}

@@ -12,7 +12,8 @@ marshal arguments. ``torch_adapter`` builds descriptors from torch tensors.
 from ._binding import (  # noqa: F401
     CS_DTYPE_BF16, CS_DTYPE_F16, CS_DTYPE_F32, CS_INT8_BLOCK, CS_MAX_GROUPS,
     CS_MAX_TENSORS, CS_NOALLOC_MAX_TENSORS, CS_NOALLOC_MAX_UNITS, CS_NOALLOC_UNIT, CS_OK,
-    CS_STATE_BF16, CS_STATE_F32, CS_STATE_INT8, DTYPE_CODES,
+    CS_STATE_BF16, CS_STATE_DYN8, CS_STATE_F32, CS_STATE_INT8, CS_STATE_INT8_UV,
+    CS_TENSOR_STATE_F32, DTYPE_CODES, EIGHT_BIT,
     EXPORTS, STATE_CODES, CompactStateError, Plan, adamw_build_units, adamw_grad_prologue,
     adamw_group_t,
     adamw_plan_create, adamw_plan_destroy, adamw_plan_error, adamw_plan_info,

@@ -26,6 +26,9 @@ CS_DTYPE_F16 = 2
 CS_STATE_F32 = 0
 CS_STATE_BF16 = 1
 CS_STATE_INT8 = 2
+CS_STATE_INT8_UV = 3
+CS_STATE_DYN8 = 4
+CS_TENSOR_STATE_F32 = 1
 CS_INT8_BLOCK = 256
 CS_MAX_GROUPS = 64
 CS_MAX_TENSORS = 245760
@@ -34,7 +37,9 @@ CS_NOALLOC_MAX_UNITS = 65536
 CS_NOALLOC_UNIT = 49152
 
 DTYPE_CODES = {"f32": CS_DTYPE_F32, "bf16": CS_DTYPE_BF16, "f16": CS_DTYPE_F16}
-STATE_CODES = {"f32": CS_STATE_F32, "bf16": CS_STATE_BF16, "int8": CS_STATE_INT8}
+STATE_CODES = {"f32": CS_STATE_F32, "bf16": CS_STATE_BF16, "int8": CS_STATE_INT8,
+               "int8uv": CS_STATE_INT8_UV, "dyn8": CS_STATE_DYN8}
+EIGHT_BIT = ("int8", "int8uv", "dyn8")
 
 
 class adamw_group_t(ctypes.Structure):
@@ -48,7 +53,8 @@ class adamw_tensor_t(ctypes.Structure):
                 ("m", ctypes.c_void_p), ("v", ctypes.c_void_p),
                 ("m_scale", ctypes.c_void_p), ("v_scale", ctypes.c_void_p),
                 ("numel", ctypes.c_int64), ("param_dtype", ctypes.c_int32),
-                ("group", ctypes.c_int32), ("master", ctypes.c_void_p)]
+                ("group", ctypes.c_int32), ("master", ctypes.c_void_p),
+                ("flags", ctypes.c_int32)]
 
 
 class adamw_plan_info_t(ctypes.Structure):
@@ -162,9 +168,10 @@ def adamw_strerror(code: int) -> str:
 
 def tensor_desc(param, grad, m, v, m_scale=None, v_scale=None, group: int = 0,
                 numel: Optional[int] = None, param_dtype: Optional[str] = None,
-                master=None) -> adamw_tensor_t:
+                master=None, flags: int = 0) -> adamw_tensor_t:
     """An ``adamw_tensor_t`` from torch tensors (or int addresses + numel/dtype);
-    ``master``: optional fp32 master weights of a 16-bit param."""
+    ``master``: optional fp32 master weights of a 16-bit param; ``flags``:
+    CS_TENSOR_* bits."""
     if numel is None:
         numel = int(param.numel())
     if param_dtype is None:
@@ -172,7 +179,7 @@ def tensor_desc(param, grad, m, v, m_scale=None, v_scale=None, group: int = 0,
                        "torch.float16": "f16"}[str(param.dtype)]
     return adamw_tensor_t(_ptr(param), _ptr(grad), _ptr(m), _ptr(v), _ptr(m_scale),
                           _ptr(v_scale), int(numel), DTYPE_CODES[param_dtype], int(group),
-                          _ptr(master))
+                          _ptr(master), int(flags))
 
 
 def adamw_plan_create(tensors: Sequence[adamw_tensor_t], state_kind="f32",

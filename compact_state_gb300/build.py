@@ -18,7 +18,9 @@ INCLUDE = os.path.join(ROOT, "include")
 LIB_NAME = "libcompact_state.so"
 LIB_PATH = os.path.join(PKG, LIB_NAME)
 BUILD_DIR = os.path.join(PKG, "_build")
-SOURCES = ("plan.cu", "adamw_kernels.cu", "noalloc.cu", "prologue.cu")
+SOURCES = ("plan.cu", "noalloc.cu", "prologue.cu", "step_launch.cu", "step_kernel_f32.cu",
+           "step_kernel_bf16.cu", "step_kernel_int8.cu", "step_kernel_int8uv.cu",
+           "step_kernel_dyn8.cu")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 CFLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC,-O2",
           "--expt-relaxed-constexpr", "-I", INCLUDE, "-I", CSRC]

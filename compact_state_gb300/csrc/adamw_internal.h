@@ -1,5 +1,5 @@
 // Internal layouts shared by the host plan builder (plan.cu) and the kernels
-// (adamw_kernels.cu). Not part of the public ABI.
+// (step_kernel.cuh). Not part of the public ABI.
 #pragma once
 
 #include <cstdint>
@@ -22,8 +22,14 @@ constexpr int kProducerWarps = 2;                      // tile publisher + unit 
 constexpr int kStageBudget = 216 * 1024;               // dynamic shared memory for stages
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;     // 2 s bound on every wait
 
+// The 8-bit state kinds share one kernel shape (one 256-element block per
+// compute warp, one byte per moment element).
+constexpr bool is_8bit(int state_kind) {
+  return state_kind == CS_STATE_INT8 || state_kind == CS_STATE_INT8_UV ||
+         state_kind == CS_STATE_DYN8;
+}
 constexpr int consumer_warps(int state_kind) {
-  return state_kind == CS_STATE_INT8 ? CS_WARPS_INT8 : CS_WARPS_ELEMENTWISE;
+  return is_8bit(state_kind) ? CS_WARPS_INT8 : CS_WARPS_ELEMENTWISE;
 }
 constexpr int block_threads(int state_kind) {
   return 32 * (kProducerWarps + consumer_warps(state_kind));
@@ -31,8 +37,8 @@ constexpr int block_threads(int state_kind) {
 // Elements per pipeline stage: one 4-element group per compute thread for
 // fp32/bf16 moments, one 256-element block per compute warp for int8.
 constexpr int tile_elems(int state_kind) {
-  return state_kind == CS_STATE_INT8 ? consumer_warps(state_kind) * kInt8Block
-                                     : consumer_warps(state_kind) * 32 * 4;
+  return is_8bit(state_kind) ? consumer_warps(state_kind) * kInt8Block
+                             : consumer_warps(state_kind) * 32 * 4;
 }
 // Bytes of one pipeline stage for a state kind (params sized for fp32, the
 // widest param type, since the param type varies per tensor).
@@ -85,6 +91,7 @@ enum : uint8_t {
   kBulk = 2,   // every buffer 16-byte aligned: bulk (TMA) copies
   kBulkScale = 4,  // int8 scale arrays 16-byte aligned
   kMaster = 8,     // theta lives in `master` (fp32); param is its 16-bit copy
+  kStateF32 = 16,  // 8-bit plan: this tensor keeps fp32 moments (direct path)
 };
 // How a tile reads and writes theta: the param dtype, or an fp32 master with
 // a 16-bit copy (kThetaMasterBF16 / kThetaMasterF16 = dtype + 2).
@@ -140,8 +147,9 @@ TensorDesc make_desc(const adamw_tensor_t& t, int32_t state_kind, uint8_t flags)
 int check_group(const adamw_group_t& g);
 }  // namespace host
 
-// Launch one step. Defined in adamw_kernels.cu. `master`: some tensor of the
-// launch has fp32 master weights (selects the kernel built with those modes).
+// Launch one step. Defined in step_launch.cu. `master`: some tensor of the
+// launch has fp32 master weights or (8-bit plans) fp32 moments; selects the
+// kernel built with those cases.
 cudaError_t launch_step(int state_kind, ArgClass cls, bool master, const void* args,
                         int grid, cudaStream_t stream);
 // Max resident CTAs per SM of the kernel for (state_kind, cls); also sets the

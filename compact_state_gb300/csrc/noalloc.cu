@@ -40,7 +40,7 @@ constexpr int kNaMaxDevices = 64;
 struct NaDevice {
   bool ready;
   unsigned char* scratch;   // device address of g_noalloc_scratch on this device
-  int grid[3][3];           // persistent grid per [state kind][argument class]
+  int grid[5][3];           // persistent grid per [state kind][argument class]
 };
 NaDevice g_dev[kNaMaxDevices];
 std::mutex g_mu;                              // guards set-up and the host staging
@@ -61,7 +61,7 @@ int setup_device(int dev, NaDevice** out) {
     int sms = 0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return CS_ERR_CUDA;
-    for (int sk = 0; sk < 3; ++sk)
+    for (int sk = 0; sk < 5; ++sk)
       for (int c = 0; c < 3; ++c) {
         int per_sm = 0;
         if (step_kernel_occupancy(sk, static_cast<ArgClass>(c), &per_sm) != cudaSuccess ||
@@ -139,7 +139,7 @@ extern "C" int adamw_step_noalloc(const adamw_tensor_t* tensors, int32_t n_tenso
     if (nu + units > kNaMaxUnits) return CS_ERR_LIMIT;
     TensorDesc& d = g_stage_descs[i];
     d = host::make_desc(t, state_kind, flags);
-    any_master = any_master || t.master != nullptr;
+    any_master = any_master || t.master != nullptr || (flags & kStateF32) != 0;
     d.n_units = static_cast<int32_t>(units);
     for (int64_t k = 0; k < units; ++k) {
       WorkUnit& w = g_stage_units[nu + k];

@@ -20,7 +20,7 @@ struct adamw_plan {
   int32_t unit_elems = 0;
   int32_t max_group = 0;
   int32_t sm_count = 0;
-  bool any_master = false;         // some tensor has fp32 master weights
+  bool any_master = false;         // some tensor has fp32 masters or fp32 moments in an 8-bit plan
   int64_t n_units = 0;
   int64_t total_numel = 0;
   int64_t device_bytes = 0;
@@ -59,6 +59,8 @@ int state_elem_bytes(int32_t kind) {
     case CS_STATE_F32: return 4;
     case CS_STATE_BF16: return 2;
     case CS_STATE_INT8: return 1;
+    case CS_STATE_INT8_UV: return 1;
+    case CS_STATE_DYN8: return 1;
     default: return 0;
   }
 }
@@ -70,7 +72,9 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 // master when there is one; param is then only stored, four at a time).
 uint8_t access_flags(const adamw_tensor_t& t, int32_t state_kind) {
   const int pb = elem_bytes(t.param_dtype);
-  const int sb = state_elem_bytes(state_kind);
+  const bool f32_state = (t.flags & CS_TENSOR_STATE_F32) != 0;
+  const bool coded = cs::is_8bit(state_kind) && !f32_state;
+  const int sb = f32_state ? 4 : state_elem_bytes(state_kind);
   const bool vec_core = aligned(t.param, 4 * pb) && aligned(t.grad, 4 * pb) &&
                         aligned(t.m, 4 * sb) && aligned(t.v, 4 * sb);
   const bool bulk_core = aligned(t.grad, 16) && aligned(t.m, 16) && aligned(t.v, 16);
@@ -83,8 +87,8 @@ uint8_t access_flags(const adamw_tensor_t& t, int32_t state_kind) {
     if (vec_core) f |= cs::kVec;
     if (bulk_core && aligned(t.param, 16)) f |= cs::kBulk;
   }
-  if (state_kind == CS_STATE_INT8 && aligned(t.m_scale, 16) && aligned(t.v_scale, 16))
-    f |= cs::kBulkScale;
+  if (coded && aligned(t.m_scale, 16) && aligned(t.v_scale, 16)) f |= cs::kBulkScale;
+  if (f32_state) f |= cs::kStateF32;
   return f;
 }
 
@@ -95,15 +99,18 @@ int check_tensor(const adamw_tensor_t& t, int32_t state_kind, uint8_t* flags) {
   if (pb == 0) return CS_ERR_UNSUPPORTED;
   if (t.group >= CS_MAX_GROUPS) return CS_ERR_LIMIT;
   if (t.master && t.param_dtype == CS_DTYPE_F32) return CS_ERR_INVALID_ARGUMENT;
-  *flags = t.master ? cs::kMaster : 0;
+  if (t.flags & ~CS_TENSOR_STATE_F32) return CS_ERR_INVALID_ARGUMENT;
+  const bool f32_state = (t.flags & CS_TENSOR_STATE_F32) != 0;
+  if (f32_state && !cs::is_8bit(state_kind)) return CS_ERR_INVALID_ARGUMENT;
+  *flags = static_cast<uint8_t>((t.master ? cs::kMaster : 0) | (f32_state ? cs::kStateF32 : 0));
   if (t.numel == 0) return CS_OK;
   if (t.numel > (int64_t(1) << 40)) return CS_ERR_LIMIT;
-  const int sb = state_elem_bytes(state_kind);
+  const int sb = f32_state ? 4 : state_elem_bytes(state_kind);
   if (!t.param || !t.grad || !t.m || !t.v) return CS_ERR_INVALID_ARGUMENT;
   if (!aligned(t.param, pb) || !aligned(t.grad, pb) || !aligned(t.m, sb) || !aligned(t.v, sb))
     return CS_ERR_MISALIGNED;
   if (t.master && !aligned(t.master, 4)) return CS_ERR_MISALIGNED;
-  if (state_kind == CS_STATE_INT8) {
+  if (cs::is_8bit(state_kind) && !f32_state) {
     if (!t.m_scale || !t.v_scale) return CS_ERR_INVALID_ARGUMENT;
     if (!aligned(t.m_scale, 4) || !aligned(t.v_scale, 4)) return CS_ERR_MISALIGNED;
   }
@@ -118,8 +125,9 @@ TensorDesc make_desc(const adamw_tensor_t& t, int32_t state_kind, uint8_t flags)
   d.grad = t.grad;
   d.m = t.m;
   d.v = t.v;
-  d.m_scale = state_kind == CS_STATE_INT8 ? t.m_scale : nullptr;
-  d.v_scale = state_kind == CS_STATE_INT8 ? t.v_scale : nullptr;
+  const bool coded = cs::is_8bit(state_kind) && !(t.flags & CS_TENSOR_STATE_F32);
+  d.m_scale = coded ? t.m_scale : nullptr;
+  d.v_scale = coded ? t.v_scale : nullptr;
   d.master = t.master;
   d.group = static_cast<int16_t>(t.group);
   d.param_dtype = static_cast<uint8_t>(t.param_dtype);
@@ -280,7 +288,8 @@ int adamw_state_bytes(const int64_t* numels, int32_t n_tensors, int32_t state_ki
     const int64_t n = numels[i];
     if (n < 0) return CS_ERR_INVALID_ARGUMENT;
     total += 2 * sb * n + 4;   // two moments + a 4-byte step counter
-    if (state_kind == CS_STATE_INT8) total += 2 * 4 * ((n + cs::kInt8Block - 1) / cs::kInt8Block);
+    if (cs::is_8bit(state_kind))
+      total += 2 * 4 * ((n + cs::kInt8Block - 1) / cs::kInt8Block);
   }
   *out_bytes = total;
   return CS_OK;
@@ -339,7 +348,7 @@ int adamw_plan_create(const adamw_tensor_t* tensors, int32_t n_tensors, int32_t 
       rc = check_tensor(t, state_kind, &vec);
       if (rc) { delete p; return rc; }
       p->h_descs[i] = make_desc(t, state_kind, vec);
-      p->any_master = p->any_master || t.master != nullptr;
+      p->any_master = p->any_master || t.master != nullptr || (vec & cs::kStateF32) != 0;
       numels[i] = t.numel;
       p->total_numel += t.numel;
       p->max_group = std::max(p->max_group, t.group);
@@ -509,6 +518,7 @@ int adamw_plan_set_grads(adamw_plan_t* p, const void* const* grads, struct CUstr
     t.v_scale = d.v_scale;
     t.master = d.master;
     t.param_dtype = d.param_dtype;
+    t.flags = (d.flags & cs::kStateF32) ? CS_TENSOR_STATE_F32 : 0;
     d.flags = access_flags(t, p->state_kind);
   }
   std::memcpy(p->h_staging, p->h_descs.data(), bytes);

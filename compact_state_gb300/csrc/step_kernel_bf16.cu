@@ -1,0 +1,5 @@
+// Step kernels with CS_STATE_BF16 moments (all argument classes, with and without
+// master weights); the kernel itself is in step_kernel.cuh.
+#include "step_kernel.cuh"
+
+CS_STEP_KERNEL_TU(bf16, CS_STATE_BF16)

@@ -10,10 +10,17 @@ from typing import List, Optional, Sequence
 
 import torch
 
-from ._binding import (CS_INT8_BLOCK, Plan, adamw_grad_prologue, adamw_plan_create,
-                       adamw_plan_set_grads, adamw_step, pack_present, tensor_desc)
+from ._binding import (CS_INT8_BLOCK, CS_TENSOR_STATE_F32, EIGHT_BIT, Plan,
+                       adamw_grad_prologue, adamw_plan_create, adamw_plan_set_grads,
+                       adamw_step, pack_present, tensor_desc)
 
-STATE_TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "int8": torch.int8}
+# storage dtype of (m, v) per state kind (8-bit codes are raw bytes)
+STATE_TORCH_DTYPES = {"f32": (torch.float32, torch.float32),
+                      "bf16": (torch.bfloat16, torch.bfloat16),
+                      "int8": (torch.int8, torch.int8),
+                      "int8uv": (torch.int8, torch.uint8),
+                      "dyn8": (torch.uint8, torch.uint8)}
+STATE_TORCH_DTYPE = {k: v[0] for k, v in STATE_TORCH_DTYPES.items()}
 
 
 class AdamWState:
@@ -24,11 +31,13 @@ class AdamWState:
     master: keep fp32 master weights for the 16-bit params (initialised to
     their exact fp32 values); the step then updates the master and writes
     each 16-bit param as its rounding.
+    min_8bit_size: with an 8-bit state kind, tensors with fewer elements keep
+    fp32 moments (``fp32_state[i]`` tells which).
     """
 
     def __init__(self, params: Sequence[torch.Tensor], grads: Sequence[torch.Tensor],
                  state_kind: str = "f32", group_of: Optional[Sequence[int]] = None,
-                 unit_elems: int = 0, master: bool = False):
+                 unit_elems: int = 0, master: bool = False, min_8bit_size: int = 0):
         if len(params) != len(grads):
             raise ValueError("params and grads differ in length")
         self.params = list(params)
@@ -36,21 +45,24 @@ class AdamWState:
         self.state_kind = state_kind
         n = len(self.params)
         self.group_of = list(group_of) if group_of is not None else [0] * n
-        sdt = STATE_TORCH_DTYPE[state_kind]
+        mdt, vdt = STATE_TORCH_DTYPES[state_kind]
         dev = self.params[0].device if n else torch.device("cuda")
         self.m: List[torch.Tensor] = []
         self.v: List[torch.Tensor] = []
         self.m_scale: List[Optional[torch.Tensor]] = []
         self.v_scale: List[Optional[torch.Tensor]] = []
         self.master: List[Optional[torch.Tensor]] = []
+        self.fp32_state: List[bool] = []
         descs = []
         for p, g, grp in zip(self.params, self.grads, self.group_of):
             if p.numel() != g.numel() or p.dtype != g.dtype:
                 raise ValueError("grad must match its param in numel and dtype")
             ne = p.numel()
-            m = torch.zeros(ne, dtype=sdt, device=dev)
-            v = torch.zeros(ne, dtype=sdt, device=dev)
-            if state_kind == "int8":
+            f32 = state_kind in EIGHT_BIT and ne < min_8bit_size
+            m = torch.zeros(ne, dtype=torch.float32 if f32 else mdt, device=dev)
+            v = torch.zeros(ne, dtype=torch.float32 if f32 else vdt, device=dev)
+            self.fp32_state.append(f32)
+            if state_kind in EIGHT_BIT and not f32:
                 nb = -(-ne // CS_INT8_BLOCK)
                 ms = torch.zeros(max(nb, 1), dtype=torch.float32, device=dev)
                 vs = torch.zeros(max(nb, 1), dtype=torch.float32, device=dev)
@@ -64,7 +76,8 @@ class AdamWState:
             if master and p.dtype != torch.float32:
                 mw = p.detach().reshape(-1).to(torch.float32)
             self.master.append(mw)
-            descs.append(tensor_desc(p, g, m, v, ms, vs, group=grp, master=mw))
+            descs.append(tensor_desc(p, g, m, v, ms, vs, group=grp, master=mw,
+                                     flags=CS_TENSOR_STATE_F32 if f32 else 0))
         self.step = torch.zeros(max(n, 1), dtype=torch.int32, device=dev)
         self.plan: Plan = adamw_plan_create(descs, state_kind, unit_elems)
 

@@ -73,6 +73,24 @@ struct CUstream_st;              /* cudaStream_t is `struct CUstream_st *` */
 #define CS_STATE_BF16  1         /* two bf16 moments per element (RNE)      */
 #define CS_STATE_INT8  2         /* two int8 codes per element + two fp32
                                     scales per 256-element block            */
+/* 8-bit variants ("Fused Optimizers and State Precision", section 05: real
+ * 8-bit optimizers may use other codebooks than the uniform teaching codec).
+ * Same layout as CS_STATE_INT8: one byte per element per moment, one fp32
+ * scale per 256-element block per moment.                                   */
+#define CS_STATE_INT8_UV 3       /* m as CS_STATE_INT8; v unsigned: codes
+                                    0..255, scale = max|v| / 255            */
+#define CS_STATE_DYN8  4         /* dynamic-exponent codebook (dynamic tree
+                                    quantization): m signed map (sign bit,
+                                    base-10 exponent as leading zeros,
+                                    indicator bit, linear fraction), v the
+                                    unsigned map; scale = block max|x|; the
+                                    code is the nearest table value        */
+
+/* adamw_tensor_t.flags */
+#define CS_TENSOR_STATE_F32  1   /* in an 8-bit plan, keep fp32 moments for
+                                    this tensor (m, v: numel fp32 values, no
+                                    scales): the selective high precision
+                                    section 05 cites for small tensors      */
 
 #define CS_INT8_BLOCK        256     /* elements per int8 scale block       */
 #define CS_MAX_GROUPS        64      /* parameter groups per step           */
@@ -113,6 +131,8 @@ typedef struct adamw_tensor_t {
                             The caller initialises it, usually to param's
                             exact fp32 value. A master on an fp32 param is
                             CS_ERR_INVALID_ARGUMENT.                       */
+    int32_t     flags;   /* CS_TENSOR_* bits (0: none). CS_TENSOR_STATE_F32
+                            outside an 8-bit plan is CS_ERR_INVALID_ARGUMENT */
 } adamw_tensor_t;
 
 /* Moments start at zero: the caller zero-fills m and v (and, for int8, the

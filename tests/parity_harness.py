@@ -36,6 +36,7 @@ from oracle import formats as ofmt
 from oracle.adamw import TensorState, new_state, oracle_step
 
 F32_RTOL = 2e-6
+EIGHT_BIT = ("int8", "int8uv", "dyn8")
 
 
 # --------------------------------------------------------------------- metrics
@@ -149,7 +150,8 @@ class Harness:
     def __init__(self, wl: workloads.Workload, state_kind: str, unit_elems: int = 0,
                  sample: Optional[int] = None, grad_device: str = "cpu",
                  param_device_init: str = "cpu", misalign: bool = False,
-                 device: str = "cuda", seed: int = 0, master: bool = False):
+                 device: str = "cuda", seed: int = 0, master: bool = False,
+                 min_8bit_size: int = 0):
         from compact_state_gb300.torch_adapter import AdamWState
         self.wl = wl
         self.kind = state_kind
@@ -176,7 +178,10 @@ class Harness:
             self.grads.append(g)
         self.master = master
         self.state = AdamWState(self.params, self.grads, state_kind,
-                                [t.group for t in wl.tensors], unit_elems, master=master)
+                                [t.group for t in wl.tensors], unit_elems, master=master,
+                                min_8bit_size=min_8bit_size)
+        # per-tensor state kind: fp32 for tensors an 8-bit plan keeps in fp32
+        self.kinds = ["f32" if f else state_kind for f in self.state.fp32_state]
         if misalign:
             # moments of the misaligned case start one element into a buffer too
             self._misalign_state(pdt)
@@ -187,7 +192,7 @@ class Harness:
             ne = spec.numel
             if sample is None or ne <= sample:
                 self.idx.append(np.arange(ne, dtype=np.int64))
-            elif state_kind == "int8":
+            elif state_kind in EIGHT_BIT:
                 nb = -(-ne // 256)
                 k = max(1, sample // 256)
                 blocks = np.sort(rng.choice(nb, size=min(k, nb), replace=False))
@@ -204,7 +209,7 @@ class Harness:
         self.ostates: List[TensorState] = []
         for i, spec in enumerate(wl.tensors):
             th = torch_to_f64(self.params[i].view(-1)[self.tidx[i]])
-            self.ostates.append(new_state(th, self.fmt, state_kind, group=spec.group,
+            self.ostates.append(new_state(th, self.fmt, self.kinds[i], group=spec.group,
                                           master=master))
         self.gpu_groups = self._gpu_groups()
         self.inv_scale_t = torch.tensor([wl.inv_scale], dtype=torch.float32, device=self.dev)
@@ -216,11 +221,10 @@ class Harness:
         from compact_state_gb300 import adamw_plan_create, adamw_plan_destroy, tensor_desc
         st = self.state
         adamw_plan_destroy(st.plan)
-        sdt = {"f32": torch.float32, "bf16": torch.bfloat16, "int8": torch.int8}[self.kind]
         descs = []
         for i, spec in enumerate(self.wl.tensors):
-            bm = torch.zeros(spec.numel + 1, dtype=sdt, device=self.dev)
-            bv = torch.zeros(spec.numel + 1, dtype=sdt, device=self.dev)
+            bm = torch.zeros(spec.numel + 1, dtype=st.m[i].dtype, device=self.dev)
+            bv = torch.zeros(spec.numel + 1, dtype=st.v[i].dtype, device=self.dev)
             self._storage += [bm, bv]
             st.m[i], st.v[i] = bm[1:], bv[1:]
             if st.master[i] is not None:
@@ -230,7 +234,8 @@ class Harness:
                 st.master[i] = bw[1:]
             descs.append(tensor_desc(self.params[i], self.grads[i], st.m[i], st.v[i],
                                      st.m_scale[i], st.v_scale[i], group=spec.group,
-                                     master=st.master[i]))
+                                     master=st.master[i],
+                                     flags=1 if st.fp32_state[i] else 0))
         st.plan = adamw_plan_create(descs, self.kind, 0)
 
     def _gpu_groups(self):
@@ -269,7 +274,7 @@ class Harness:
             self.params[i].view(-1)[ix] = f64_to_torch(o.theta, pdt, self.dev)
             if o.master is not None:
                 st.master[i][ix] = f64_to_torch(o.master, torch.float32, self.dev)
-            if self.kind == "int8":
+            if o.state_kind in EIGHT_BIT:
                 st.m[i][ix] = torch.from_numpy(o.m).to(self.dev)
                 st.v[i][ix] = torch.from_numpy(o.v).to(self.dev)
                 blk = torch.unique(ix // 256)
@@ -278,7 +283,7 @@ class Harness:
                 st.v_scale[i][blk] = torch.from_numpy(o.v_scale).to(self.dev)[
                     self._oblk(i, blk)]
             else:
-                sdt = torch.float32 if self.kind == "f32" else torch.bfloat16
+                sdt = st.m[i].dtype
                 st.m[i][ix] = f64_to_torch(o.m, sdt, self.dev)
                 st.v[i][ix] = f64_to_torch(o.v, sdt, self.dev)
             steps[i] = o.step
@@ -296,7 +301,7 @@ class Harness:
         st = self.state
         ix = self.tidx[i]
         th = torch_to_f64(self.params[i].view(-1)[ix])
-        if self.kind == "int8":
+        if self.kinds[i] in EIGHT_BIT:
             m = st.m[i][ix].cpu().numpy()
             v = st.v[i][ix].cpu().numpy()
             blk = torch.from_numpy(np.unique(self.idx[i] // 256)).to(self.dev)
@@ -390,19 +395,22 @@ class Harness:
                 upd("theta_ulp", ulp_diff(th, o.theta, self.fmt).max(initial=0))
                 th16.append(th)
                 th16r.append(o.theta)
-            if self.kind == "f32":
+            kind = self.kinds[i]
+            if kind == "f32":
                 # fp32 bar relative to the rms over every compared position: a
                 # single-element tensor near a zero crossing has no scale of its own
                 mv["m"][0].append(m)
                 mv["m"][1].append(o.m)
                 mv["v"][0].append(v)
                 mv["v"][1].append(o.v)
-            elif self.kind == "bf16":
+            elif kind == "bf16":
                 upd("m_ulp", ulp_diff(m, o.m, "bf16").max(initial=0))
                 upd("v_ulp", ulp_diff(v, o.v, "bf16").max(initial=0))
             else:
-                upd("m_code", np.abs(m.astype(int) - o.m.astype(int)).max(initial=0))
-                upd("v_code", np.abs(v.astype(int) - o.v.astype(int)).max(initial=0))
+                upd("m_code", np.abs(code_index(m, kind, "m") -
+                                     code_index(o.m, kind, "m")).max(initial=0))
+                upd("v_code", np.abs(code_index(v, kind, "v") -
+                                     code_index(o.v, kind, "v")).max(initial=0))
                 upd("m_scale_rel", _scale_rel(ms, o.m_scale))
                 upd("v_scale_rel", _scale_rel(vs, o.v_scale))
         if th_all:
@@ -443,17 +451,29 @@ def _bits_equal(a: torch.Tensor, b: torch.Tensor) -> bool:
     return torch.equal(a.contiguous().view(view), b.contiguous().view(view))
 
 
+def code_index(codes, kind: str, which: str) -> np.ndarray:
+    """Codes as positions on their codebook's axis, so neighbouring values
+    differ by one: signed linear codes as themselves, unsigned bytes as
+    0..255, signed codebook bytes (sign<<7 | r) as +-r."""
+    c = np.asarray(codes)
+    if kind == "dyn8" and which == "m":
+        b = c.astype(np.uint8).astype(np.int64)
+        return np.where(b & 0x80, -(b & 0x7F), b & 0x7F)
+    return c.astype(np.int64)
+
+
 def check_bars(res: Result, kind: str, fmt: str, forced: bool) -> None:
-    """Assert the tolerances for the mode that ran."""
+    """Assert the tolerances for the mode that ran: every key present must
+    meet its bar, and the keys of the state kind and param format must be
+    there (so a comparison that did not run cannot pass)."""
     w = res.forced if forced else res.free
-    assert w.get("theta_excess", 0) <= 1.0, w       # fp32 params, or fp32 masters
-    if fmt != "f32":
-        assert w.get("theta16_excess", 0) <= 1.0, w
-    assert w.get("copy_mismatch", 0) == 0, w
-    if kind == "f32":
-        assert w.get("m_excess", 0) <= 1.0 and w.get("v_excess", 0) <= 1.0, w
-    elif kind == "bf16":
-        assert w.get("m_ulp", 0) <= 1 and w.get("v_ulp", 0) <= 1, w
-    else:
-        assert w.get("m_code", 0) <= 1 and w.get("v_code", 0) <= 1, w
-        assert w.get("m_scale_rel", 0) <= 1e-6 and w.get("v_scale_rel", 0) <= 1e-6, w
+    bars = {"theta_excess": 1.0, "theta16_excess": 1.0, "m_excess": 1.0, "v_excess": 1.0,
+            "m_ulp": 1, "v_ulp": 1, "m_code": 1, "v_code": 1, "m_scale_rel": 1e-6,
+            "v_scale_rel": 1e-6, "copy_mismatch": 0}
+    need = {"f32": ["m_excess", "v_excess"], "bf16": ["m_ulp", "v_ulp"]}.get(
+        kind, ["m_code", "v_code", "m_scale_rel", "v_scale_rel"])
+    need = need + (["theta_excess"] if fmt == "f32" else ["theta16_excess"])
+    for k in need:
+        assert k in w, (k, w)
+    for k, bar in bars.items():
+        assert w.get(k, 0) <= bar, (k, w)

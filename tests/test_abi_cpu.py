@@ -70,14 +70,14 @@ def test_strerror_names_every_code(cs):
     assert cs.adamw_strerror(-99) == "unknown status"
 
 
-@pytest.mark.parametrize("kind", ["f32", "bf16", "int8"])
+@pytest.mark.parametrize("kind", ["f32", "bf16", "int8", "int8uv", "dyn8"])
 def test_state_bytes_equals_oracle_ledger(cs, kind):
     rng = np.random.default_rng(0)
     numels = [0, 1, 255, 256, 257] + list(rng.integers(1, 10 ** 6, 50))
     assert cs.adamw_state_bytes(numels, kind) == ostate.state_bytes(numels, kind)
     lora = workloads.lora()
     mib = round(cs.adamw_state_bytes(lora.numels, kind) / 2 ** 20, 3)
-    assert mib == {"f32": 185.501, "bf16": 92.751, "int8": 47.101}[kind]
+    assert mib == {"f32": 185.501, "bf16": 92.751}.get(kind, 47.101)
 
 
 def test_state_bytes_rejects_bad_input(cs):
@@ -86,6 +86,7 @@ def test_state_bytes_rejects_bad_input(cs):
     with pytest.raises(KeyError):
         cs.adamw_state_bytes([5], "f8")
     assert cs.lib().adamw_state_bytes(None, 0, 7, ctypes.byref(ctypes.c_int64())) == -2
+    assert cs.lib().adamw_state_bytes(None, 0, 5, ctypes.byref(ctypes.c_int64())) == -2
 
 
 @pytest.mark.parametrize("unit", [256, 1024, 32768])
@@ -135,6 +136,11 @@ def _desc(cs, **kw):
     (dict(v_scale=0x60002), "int8", -3),
     (dict(master=0x70000), "f32", -1),        # a master needs a 16-bit param
     (dict(master=0x70002, param_dtype=1), "f32", -3),   # master not 4-byte aligned
+    (dict(flags=2), "int8", -1),                        # unknown tensor flag
+    (dict(flags=1), "f32", -1),                         # fp32 moments outside an 8-bit plan
+    (dict(flags=1, m=0x30002), "dyn8", -3),             # fp32 moments need 4-byte alignment
+    (dict(m_scale=0), "int8uv", -1),
+    (dict(v_scale=0x60002), "dyn8", -3),
 ])
 def test_plan_create_rejects_invalid_tensors(cs, kw, state, code):
     arr = (cs.adamw_tensor_t * 2)(_desc(cs), _desc(cs, **kw))
@@ -149,7 +155,7 @@ def test_plan_create_rejects_bad_arguments(cs):
     out = ctypes.c_void_p()
     assert L.adamw_plan_create(None, 1, 0, 0, ctypes.byref(out)) == -1
     assert L.adamw_plan_create(arr, 0, 0, 0, ctypes.byref(out)) == -1
-    assert L.adamw_plan_create(arr, 1, 3, 0, ctypes.byref(out)) == -2
+    assert L.adamw_plan_create(arr, 1, 5, 0, ctypes.byref(out)) == -2
     assert L.adamw_plan_create(arr, 1, 0, 100, ctypes.byref(out)) == -1
     assert L.adamw_plan_create(arr, 1, 0, 0, None) == -1
     assert L.adamw_plan_create(arr, 245761, 0, 0, ctypes.byref(out)) == -4
@@ -175,5 +181,17 @@ def test_valid_plan_without_gpu_reports_cuda_error(cs):
 
 def test_tensor_struct_layout_matches_header(cs):
     # the C struct: six pointers, int64 numel, two int32, then the master pointer
-    assert ctypes.sizeof(cs.adamw_tensor_t) == 72
+    assert ctypes.sizeof(cs.adamw_tensor_t) == 80
     assert cs.adamw_tensor_t.master.offset == 64
+    assert cs.adamw_tensor_t.flags.offset == 72
+
+
+def test_selective_fp32_tensor_needs_no_scales(cs):
+    # an fp32-moment tensor in an 8-bit plan validates without scale arrays
+    # (then fails only for want of a GPU here)
+    arr = (cs.adamw_tensor_t * 1)(_desc(cs, m_scale=0, v_scale=0, flags=1))
+    out = ctypes.c_void_p()
+    rc = cs.lib().adamw_plan_create(arr, 1, cs.STATE_CODES["dyn8"], 0, ctypes.byref(out))
+    assert rc in (0, -5)
+    if rc == 0:
+        cs.adamw_plan_destroy(cs.Plan(out.value, 1))

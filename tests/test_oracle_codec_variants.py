@@ -173,3 +173,17 @@ def test_codebook_negative_zero_never_produced():
     x = np.concatenate([[1.0], -np.full(255, 1e-9)])   # rounds to zero magnitude
     q, _ = dynamic8.encode_signed(x)
     assert np.all(q[1:] == 0)
+
+
+@pytest.mark.parametrize("mid,first_exp,mbits", [(dynamic8.SIGNED_MID, -21, 6),
+                                                  (dynamic8.UNSIGNED_MID, -25, 7)])
+def test_codebook_midpoints_one_per_fine_bucket(mid, first_exp, mbits):
+    """Cut [2^first_exp, 1) into 2^mbits equal buckets per binary octave: each
+    holds at most one midpoint of the map, and everything below holds none,
+    so a code is a bucket's first midpoint index plus one comparison."""
+    m = mid.astype(np.float32).astype(np.float64)
+    assert m[0] > 2.0 ** first_exp
+    for e in range(first_exp, 0):
+        edges = 2.0 ** e * (1 + np.arange((1 << mbits) + 1) / 2 ** mbits)
+        counts = np.histogram(m, bins=edges)[0]
+        assert counts.max() <= 1, (e, counts.max())
