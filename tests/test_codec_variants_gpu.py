@@ -127,6 +127,11 @@ def test_codec_bit_exact_with_zero_betas(kind):
     g[1] = 0.0                                                        # a zero block
     g[2, 1:128] = dynamic8.SIGNED_MID                                 # exact codebook
     g[3, 1:128] = -dynamic8.SIGNED_MID                                # midpoints (ties)
+    # exact linear-codec ties: max 127 * 2^-10 gives scale 2^-10, so
+    # x = (k + 1/2) * 2^-10 divides to a half-integer (ties to even)
+    g[4, 0] = 127.0 * 2.0 ** -10
+    g[4, 1:255] = np.arange(-126.5, 126.6, 1.0) * 2.0 ** -10
+    g[4, 255] = 0.5 * 2.0 ** -10
     g = g.reshape(-1).astype(np.float32)
     p = torch.zeros(n, dtype=torch.float32, device="cuda")
     gt = torch.from_numpy(g).cuda()
