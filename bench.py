@@ -227,7 +227,7 @@ def reference_arm(wl, state: str, steps: int, warmup: int, n: int = 1 << 18,
 
 
 # ------------------------------------------------------------------ GPU arm
-def alloc_state(wl, state, dev, master=False, min_8bit_size=0):
+def alloc_state(wl, state, dev, master=False, min_8bit_size=0, unit_elems=0):
     import torch
     import workloads
     from compact_state_gb300.torch_adapter import AdamWState
@@ -238,8 +238,8 @@ def alloc_state(wl, state, dev, master=False, min_8bit_size=0):
         p.copy_(workloads.init_param(wl, i, device=dev).reshape(-1))
         params.append(p)
     grads = [torch.empty_like(p) for p in params]
-    st = AdamWState(params, grads, state, [t.group for t in wl.tensors], master=master,
-                    min_8bit_size=min_8bit_size)
+    st = AdamWState(params, grads, state, [t.group for t in wl.tensors], unit_elems,
+                    master=master, min_8bit_size=min_8bit_size)
     return st
 
 
@@ -264,7 +264,7 @@ def run_native(args, wl, rank, world, dev):
     import compact_state_gb300 as cs
     from compact_state_gb300 import tensor_desc
     state = args.state
-    st = alloc_state(wl, state, dev, args.master, args.min_8bit_size)
+    st = alloc_state(wl, state, dev, args.master, args.min_8bit_size, args.unit_elems)
     plan_info = cs.adamw_plan_info(st.plan)
     # grad buffers: fresh seeded grads per step, cycling through a pool
     per_set = sum(g.numel() * g.element_size() for g in st.grads)
@@ -278,7 +278,7 @@ def run_native(args, wl, rank, world, dev):
                  for p, g, m, v, ms, vs, mw, f32, t in zip(
                      st.params, gs, st.m, st.v, st.m_scale, st.v_scale, st.master,
                      st.fp32_state, wl.tensors)]
-        plans.append(cs.adamw_plan_create(descs, state, 0))
+        plans.append(cs.adamw_plan_create(descs, state, args.unit_elems))
     groups = cs.groups_array([dict(lr=g.lr, beta1=g.beta1, beta2=g.beta2, eps=g.eps,
                                    weight_decay=g.weight_decay) for g in wl.groups])
     ng = len(wl.groups)
@@ -505,6 +505,8 @@ def main(argv=None):
                          "MAX_NORM) before every step and time both")
     ap.add_argument("--master", action="store_true",
                     help="fp32 master weights for the 16-bit params")
+    ap.add_argument("--unit-elems", type=int, default=0,
+                    help="elements per work unit (0: the library default)")
     ap.add_argument("--grad-sets", type=int, default=8)
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--e2e-chunk", type=int, default=1 << 22)

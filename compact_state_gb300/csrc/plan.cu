@@ -170,6 +170,36 @@ void build_units(const int64_t* numels, int32_t n, int32_t unit_elems,
                    [](const WorkUnit& a, const WorkUnit& b) { return a.len > b.len; });
 }
 
+// Finer units at the end of the queue. CTAs take units dynamically, so they
+// finish up to one unit apart; with 49152-element units that is ~15 us of one
+// CTA's bandwidth, a large part of a short step. The units holding the last
+// `waves` x `ctas` full units' worth of elements are re-cut into pieces of
+// `piece` elements (a multiple of the tile, so of the 256-element block) and
+// kept longest first. Recounts the units of each tensor.
+void split_tail(std::vector<WorkUnit>* units, std::vector<int32_t>* per_tensor, int64_t ctas,
+                int32_t unit_elems, int32_t piece, int waves) {
+  const int64_t tail_elems = static_cast<int64_t>(waves) * ctas * unit_elems;
+  size_t first = units->size();
+  int64_t acc = 0;
+  while (first > 0 && acc < tail_elems) acc += (*units)[--first].len;
+  std::vector<WorkUnit> tail;
+  for (size_t k = first; k < units->size(); ++k) {
+    const WorkUnit& w = (*units)[k];
+    if (w.len <= piece) {
+      tail.push_back(w);
+      continue;
+    }
+    for (int32_t off = 0; off < w.len; off += piece)
+      tail.push_back(WorkUnit{w.start + off, w.tensor, std::min(piece, w.len - off)});
+  }
+  std::stable_sort(tail.begin(), tail.end(),
+                   [](const WorkUnit& a, const WorkUnit& b) { return a.len > b.len; });
+  units->resize(first);
+  units->insert(units->end(), tail.begin(), tail.end());
+  std::fill(per_tensor->begin(), per_tensor->end(), 0);
+  for (const WorkUnit& w : *units) ++(*per_tensor)[w.tensor];
+}
+
 }  // namespace host
 }  // namespace cs
 
@@ -353,18 +383,21 @@ int adamw_plan_create(const adamw_tensor_t* tensors, int32_t n_tensors, int32_t 
       p->total_numel += t.numel;
       p->max_group = std::max(p->max_group, t.group);
     }
+    if (cudaGetDevice(&p->device) != cudaSuccess) { delete p; return CS_ERR_CUDA; }
+    if (cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
+      delete p; return CS_ERR_CUDA;
+    }
     std::vector<WorkUnit> units;
     std::vector<int32_t> per;
     build_units(numels.data(), n_tensors, ue, &units, &per);
+    // the last two waves of the queue in pieces of four tiles
+    const int32_t piece = std::min(ue, 4 * cs::tile_elems(state_kind));
+    split_tail(&units, &per, p->sm_count, ue, piece, 2);
     p->h_numel = numels;
     if (units.size() >= (size_t(1) << 31) - (size_t(1) << 20)) { delete p; return CS_ERR_LIMIT; }
     for (int32_t i = 0; i < n_tensors; ++i) p->h_descs[i].n_units = per[i];
     p->n_units = static_cast<int64_t>(units.size());
 
-    if (cudaGetDevice(&p->device) != cudaSuccess) { delete p; return CS_ERR_CUDA; }
-    if (cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
-      delete p; return CS_ERR_CUDA;
-    }
     for (int c = 0; c < 3; ++c) {
       int per_sm = 0;
       if (cs::step_kernel_occupancy(state_kind, static_cast<cs::ArgClass>(c), &per_sm) != cudaSuccess ||
