@@ -3,7 +3,8 @@
  *
  * One call, adamw_step(), runs one AdamW optimizer step over a whole list of
  * parameter tensors in a single persistent kernel launch. Moment state is kept
- * as fp32, compact bf16, or block-wise signed 8-bit codes.
+ * as fp32, compact bf16, or block-wise 8-bit codes (signed linear, linear with
+ * an unsigned second moment, or a dynamic-exponent codebook).
  *
  * What the step computes is the AdamW update of "Fused Optimizers and State
  * Precision" (xuujii.github.io ai-infra-kb M041), section 02, for every element
@@ -111,12 +112,14 @@ typedef struct adamw_tensor_t {
     const void *grad;    /* device, numel elements of param_dtype (stored,
                             i.e. still multiplied by the loss scale)         */
     void       *m;       /* device, first moment: numel fp32 / bf16 values,
-                            or numel int8 codes for CS_STATE_INT8            */
+                            or numel 8-bit codes for the 8-bit kinds
+                            (CS_STATE_INT8 / _INT8_UV / _DYN8), or numel fp32
+                            values for a CS_TENSOR_STATE_F32 tensor          */
     void       *v;       /* device, second moment, same layout as m          */
-    float      *m_scale; /* device, CS_STATE_INT8 only: ceil(numel/256) fp32
+    float      *m_scale; /* device, 8-bit kinds only: ceil(numel/256) fp32
                             scales of m, one per 256-element block of the
                             tensor's flat order (else ignored, may be NULL)  */
-    float      *v_scale; /* device, CS_STATE_INT8 only: scales of v          */
+    float      *v_scale; /* device, 8-bit kinds only: scales of v            */
     int64_t     numel;   /* elements, >= 0 (0: no buffer is touched, but the
                             step count still advances when it has a grad)    */
     int32_t     param_dtype;  /* CS_DTYPE_*; grad has the same dtype         */
@@ -277,8 +280,9 @@ int adamw_plan_destroy(adamw_plan_t *plan);
 
 /*
  * adamw_state_bytes -- bytes of optimizer state for a tensor list, host only:
- * moments (8 / 4 / 2 bytes per element for fp32 / bf16 / int8), plus for int8
- * two fp32 scales per 256-element block of each tensor, plus a 4-byte step
+ * moments (8 / 4 / 2 bytes per element for fp32 / bf16 / the 8-bit kinds),
+ * plus for the 8-bit kinds two fp32 scales per 256-element block of each
+ * tensor (every tensor counted in the one kind), plus a 4-byte step
  * counter per tensor. Section 05's payload ledger; the ApexW Unsloth benchmark
  * page's 185.501 / 92.751 / 47.101 MB for its LoRA set follow from it.
  *   numels  host array [n_tensors]; out: host int64.
