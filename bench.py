@@ -361,16 +361,24 @@ def run_native(args, wl, rank, world, dev):
         cs.adamw_plan_destroy(p)
     del sets
     if not args.no_e2e:
-        result["e2e"] = run_e2e(args, wl, st, groups, ng, dev, world)
+        result["e2e"] = run_e2e(args, wl, st, groups, ng, dev, world, offload=False)
+        result["e2e_offload"] = run_e2e(args, wl, st, groups, ng, dev, world, offload=True)
     return result
 
 
-def run_e2e(args, wl, st, groups, ng, dev, world):
-    """Host-resident params, grads and moments through the public API: every
-    step copies them in from pinned memory, steps, and copies params and
-    moments back. The parameter set is cut into chunks with one plan each, so
-    the copy-in of chunk i+1, the step of chunk i and the copy-out of chunk
-    i-1 overlap on three streams (both copy directions run at once)."""
+def run_e2e(args, wl, st, groups, ng, dev, world, offload=False):
+    """End to end through the public API with host buffers.
+
+    Default: the step's inputs are the gradients and its result the updated
+    params, while the optimizer state (moments, scales, step counts, fp32
+    masters) stays resident in HBM as in training. Every step copies the grads
+    in from pinned host memory and the params back out.
+    offload=True: params, grads and moments all live in pinned host memory;
+    every step copies them in and params and moments back (a fully offloaded
+    optimizer).
+    The parameter set is cut into chunks with one plan each, so the copy-in of
+    chunk i+1, the step of chunk i and the copy-out of chunk i-1 overlap on
+    three streams (both copy directions run at once)."""
     import torch
     import compact_state_gb300 as cs
     from compact_state_gb300 import tensor_desc
@@ -386,8 +394,6 @@ def run_e2e(args, wl, st, groups, ng, dev, world):
                   sl(st.m_scale[i], b0, b1), sl(st.v_scale[i], b0, b1),
                   sl(st.master[i], c0, c1)]
             chunks.append((i, dv))
-    host = [[None if d is None else d.detach().to("cpu").pin_memory() for d in dv]
-            for _, dv in chunks]
     plans = []
     for (i, dv) in chunks:
         plans.append(cs.adamw_plan_create(
@@ -396,10 +402,18 @@ def run_e2e(args, wl, st, groups, ng, dev, world):
     steps = torch.zeros(len(chunks), dtype=torch.int32, device=dev)
     inv = torch.tensor([wl.inv_scale], dtype=torch.float32, device=dev)
     # in: what the step reads (theta from the master when there is one); out:
-    # what it writes
-    in_idx = lambda dv: [j for j in ([1, 2, 3, 4, 5, 6] if dv[6] is not None
-                                     else [0, 1, 2, 3, 4, 5]) if dv[j] is not None]
-    out_idx = lambda dv: [j for j in (0, 2, 3, 4, 5, 6) if dv[j] is not None]
+    # what it writes. Without offload only the grads go in and the params out.
+    if offload:
+        in_idx = lambda dv: [j for j in ([1, 2, 3, 4, 5, 6] if dv[6] is not None
+                                         else [0, 1, 2, 3, 4, 5]) if dv[j] is not None]
+        out_idx = lambda dv: [j for j in (0, 2, 3, 4, 5, 6) if dv[j] is not None]
+    else:
+        in_idx = lambda dv: [1]
+        out_idx = lambda dv: [0]
+    # pinned host copies of the buffers that cross the link, and only those
+    host = [[dv[j].detach().to("cpu").pin_memory()
+             if dv[j] is not None and (j in in_idx(dv) or j in out_idx(dv)) else None
+             for j in range(len(dv))] for _, dv in chunks]
     nbytes = lambda h: h.numel() * h.element_size()
     h2d = sum(nbytes(host[c][j]) for c, (_, dv) in enumerate(chunks) for j in in_idx(dv))
     d2h = sum(nbytes(host[c][j]) for c, (_, dv) in enumerate(chunks) for j in out_idx(dv))
@@ -454,8 +468,10 @@ def run_e2e(args, wl, st, groups, ng, dev, world):
     return {"value": world * wl.total_numel * K / (ms / 1e3), "unit": "param-elements/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
             "ms_per_step": ms / K, "chunks": len(chunks),
-            "how": "pinned host buffers, per-chunk plans, copy-in / step / copy-out "
-                   "overlapped on three streams"}
+            "how": ("params, grads and moments in pinned host memory" if offload else
+                    "grads in from pinned host memory, params out; optimizer state "
+                    "resident in HBM") +
+                   ", per-chunk plans, copy-in / step / copy-out overlapped on three streams"}
 
 
 # ------------------------------------------------------------------ dist
@@ -567,7 +583,7 @@ def main(argv=None):
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic (seeded normal params and grads)", "config": config,
             "roofline": res["roofline"], "clocks": res["clocks"],
-            "e2e": res.get("e2e"),
+            "e2e": res.get("e2e"), "e2e_offload": res.get("e2e_offload"),
             "gpu_launches": args.steps * (2 if args.prologue is not None else 1),
             "kernel_ms_avg": res["kernel_ms_avg"], "kernel_ms_median": res["kernel_ms_median"],
             "grad_sets": res["grad_sets"], "cpu_baseline": cb}
