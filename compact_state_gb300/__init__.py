@@ -6,6 +6,7 @@ declared in ``include/compact_state.h``). This package is its thin binding:
 ``adamw_grad_prologue``, ``adamw_plan_info``, ``adamw_plan_error``,
 ``adamw_plan_set_debug``,
 ``adamw_plan_destroy``, ``adamw_state_bytes``, ``adamw_build_units``,
+``adamw_build_queue``,
 ``adamw_step_noalloc`` and ``adamw_strerror`` keep the C names and only
 marshal arguments. ``torch_adapter`` builds descriptors from torch tensors.
 """
@@ -14,7 +15,8 @@ from ._binding import (  # noqa: F401
     CS_MAX_TENSORS, CS_NOALLOC_MAX_TENSORS, CS_NOALLOC_MAX_UNITS, CS_NOALLOC_UNIT, CS_OK,
     CS_STATE_BF16, CS_STATE_DYN8, CS_STATE_F32, CS_STATE_INT8, CS_STATE_INT8_UV,
     CS_TENSOR_STATE_F32, DTYPE_CODES, EIGHT_BIT,
-    EXPORTS, STATE_CODES, CompactStateError, Plan, adamw_build_units, adamw_grad_prologue,
+    EXPORTS, STATE_CODES, CompactStateError, Plan, adamw_build_queue, adamw_build_units,
+    adamw_grad_prologue,
     adamw_group_t,
     adamw_plan_create, adamw_plan_destroy, adamw_plan_error, adamw_plan_info,
     adamw_plan_info_t, adamw_plan_set_debug,

@@ -75,7 +75,7 @@ _LIB = None
 EXPORTS = ("adamw_plan_create", "adamw_step", "adamw_plan_set_grads", "adamw_plan_info",
            "adamw_plan_destroy", "adamw_state_bytes", "adamw_build_units", "adamw_strerror",
            "adamw_plan_error", "adamw_plan_set_debug", "adamw_step_noalloc",
-           "adamw_grad_prologue")
+           "adamw_grad_prologue", "adamw_build_queue")
 
 
 def lib() -> ctypes.CDLL:
@@ -100,6 +100,9 @@ def lib() -> ctypes.CDLL:
     L.adamw_build_units.argtypes = [ctypes.POINTER(i64), i32, i32, ctypes.POINTER(i32),
                                     ctypes.POINTER(i64), ctypes.POINTER(i32), i64,
                                     ctypes.POINTER(i64)]
+    L.adamw_build_queue.argtypes = [ctypes.POINTER(i64), i32, i32, i32, i32,
+                                    ctypes.POINTER(i32), ctypes.POINTER(i64),
+                                    ctypes.POINTER(i32), i64, ctypes.POINTER(i64)]
     L.adamw_plan_error.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32)]
     L.adamw_plan_set_debug.argtypes = [vp, ctypes.c_uint64, ctypes.c_uint32]
     L.adamw_step_noalloc.argtypes = [ctypes.POINTER(adamw_tensor_t), i32, i32,
@@ -304,17 +307,31 @@ def adamw_state_bytes(numels: Sequence[int], state_kind="f32") -> int:
     return out.value
 
 
-def adamw_build_units(numels: Sequence[int], unit_elems: int = 0):
-    """(tensor, start, len) lists of the work-unit table, computed on the host."""
+def _unit_table(name, call, numels):
     n = len(numels)
     arr = (ctypes.c_int64 * max(n, 1))(*[int(x) for x in numels])
     cnt = ctypes.c_int64()
-    _check(lib().adamw_build_units(arr, n, int(unit_elems), None, None, None, 0,
-                                   ctypes.byref(cnt)), "adamw_build_units")
+    _check(call(arr, n, None, None, None, 0, ctypes.byref(cnt)), name)
     k = cnt.value
     t = (ctypes.c_int32 * max(k, 1))()
     s = (ctypes.c_int64 * max(k, 1))()
     ln = (ctypes.c_int32 * max(k, 1))()
-    _check(lib().adamw_build_units(arr, n, int(unit_elems), t, s, ln, k, ctypes.byref(cnt)),
-           "adamw_build_units")
+    _check(call(arr, n, t, s, ln, k, ctypes.byref(cnt)), name)
     return list(t[:k]), list(s[:k]), list(ln[:k])
+
+
+def adamw_build_units(numels: Sequence[int], unit_elems: int = 0):
+    """(tensor, start, len) lists of the work-unit cut, computed on the host."""
+    L = lib()
+    return _unit_table("adamw_build_units",
+                       lambda a, n, t, s, ln, cap, cnt: L.adamw_build_units(
+                           a, n, int(unit_elems), t, s, ln, cap, cnt), numels)
+
+
+def adamw_build_queue(numels: Sequence[int], state_kind, ctas: int, unit_elems: int = 0):
+    """(tensor, start, len) lists of the queue a plan builds for ``ctas`` CTAs."""
+    L = lib()
+    sk = STATE_CODES[state_kind] if isinstance(state_kind, str) else int(state_kind)
+    return _unit_table("adamw_build_queue",
+                       lambda a, n, t, s, ln, cap, cnt: L.adamw_build_queue(
+                           a, n, sk, int(unit_elems), int(ctas), t, s, ln, cap, cnt), numels)

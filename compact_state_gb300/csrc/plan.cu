@@ -200,6 +200,15 @@ void split_tail(std::vector<WorkUnit>* units, std::vector<int32_t>* per_tensor, 
   for (const WorkUnit& w : *units) ++(*per_tensor)[w.tensor];
 }
 
+// The queue a plan uses: the unit cut, then the last two waves re-cut into
+// pieces of four tiles.
+void build_queue(const int64_t* numels, int32_t n, int32_t state_kind, int32_t unit_elems,
+                 int64_t ctas, std::vector<WorkUnit>* units, std::vector<int32_t>* per_tensor) {
+  build_units(numels, n, unit_elems, units, per_tensor);
+  const int32_t piece = std::min(unit_elems, 4 * cs::tile_elems(state_kind));
+  split_tail(units, per_tensor, ctas, unit_elems, piece, 2);
+}
+
 }  // namespace host
 }  // namespace cs
 
@@ -289,6 +298,40 @@ int launch_prologue_class(adamw_plan* p, cs::ArgClass cls, const uint32_t* prese
   return cs::launch_prologue(cls, &a, grid, stream) == cudaSuccess ? CS_OK : CS_ERR_CUDA;
 }
 
+// Host-only unit tables for adamw_build_units (state_kind < 0: the plain cut)
+// and adamw_build_queue (the plan's queue for `ctas` CTAs).
+int write_units(const int64_t* numels, int32_t n_tensors, int32_t state_kind,
+                int32_t unit_elems, int32_t ctas, int32_t* tensor_out, int64_t* start_out,
+                int32_t* len_out, int64_t cap, int64_t* n_units_out) {
+  if (!n_units_out || n_tensors < 0 || (n_tensors > 0 && !numels) || cap < 0)
+    return CS_ERR_INVALID_ARGUMENT;
+  int32_t ue = 0;
+  int rc = check_unit_elems(unit_elems, &ue);
+  if (rc) return rc;
+  for (int32_t i = 0; i < n_tensors; ++i)
+    if (numels[i] < 0) return CS_ERR_INVALID_ARGUMENT;
+  try {
+    std::vector<WorkUnit> units;
+    std::vector<int32_t> per;
+    if (state_kind < 0) {
+      build_units(numels, n_tensors, ue, &units, &per);
+    } else {
+      build_queue(numels, n_tensors, state_kind, ue, ctas, &units, &per);
+    }
+    *n_units_out = static_cast<int64_t>(units.size());
+    if (static_cast<int64_t>(units.size()) > cap) return cap == 0 ? CS_OK : CS_ERR_LIMIT;
+    if (!tensor_out || !start_out || !len_out) return CS_ERR_INVALID_ARGUMENT;
+    for (size_t k = 0; k < units.size(); ++k) {
+      tensor_out[k] = units[k].tensor;
+      start_out[k] = units[k].start;
+      len_out[k] = units[k].len;
+    }
+  } catch (const std::bad_alloc&) {
+    return CS_ERR_OUT_OF_MEMORY;
+  }
+  return CS_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -328,29 +371,17 @@ int adamw_state_bytes(const int64_t* numels, int32_t n_tensors, int32_t state_ki
 int adamw_build_units(const int64_t* numels, int32_t n_tensors, int32_t unit_elems,
                       int32_t* tensor_out, int64_t* start_out, int32_t* len_out,
                       int64_t cap, int64_t* n_units_out) {
-  if (!n_units_out || n_tensors < 0 || (n_tensors > 0 && !numels) || cap < 0)
-    return CS_ERR_INVALID_ARGUMENT;
-  int32_t ue = 0;
-  int rc = check_unit_elems(unit_elems, &ue);
-  if (rc) return rc;
-  for (int32_t i = 0; i < n_tensors; ++i)
-    if (numels[i] < 0) return CS_ERR_INVALID_ARGUMENT;
-  try {
-    std::vector<WorkUnit> units;
-    std::vector<int32_t> per;
-    build_units(numels, n_tensors, ue, &units, &per);
-    *n_units_out = static_cast<int64_t>(units.size());
-    if (static_cast<int64_t>(units.size()) > cap) return cap == 0 ? CS_OK : CS_ERR_LIMIT;
-    if (!tensor_out || !start_out || !len_out) return CS_ERR_INVALID_ARGUMENT;
-    for (size_t k = 0; k < units.size(); ++k) {
-      tensor_out[k] = units[k].tensor;
-      start_out[k] = units[k].start;
-      len_out[k] = units[k].len;
-    }
-  } catch (const std::bad_alloc&) {
-    return CS_ERR_OUT_OF_MEMORY;
-  }
-  return CS_OK;
+  return write_units(numels, n_tensors, -1, unit_elems, 0, tensor_out, start_out, len_out, cap,
+                     n_units_out);
+}
+
+int adamw_build_queue(const int64_t* numels, int32_t n_tensors, int32_t state_kind,
+                      int32_t unit_elems, int32_t ctas, int32_t* tensor_out, int64_t* start_out,
+                      int32_t* len_out, int64_t cap, int64_t* n_units_out) {
+  if (state_elem_bytes(state_kind) == 0) return CS_ERR_UNSUPPORTED;
+  if (ctas < 1) return CS_ERR_INVALID_ARGUMENT;
+  return write_units(numels, n_tensors, state_kind, unit_elems, ctas, tensor_out, start_out,
+                     len_out, cap, n_units_out);
 }
 
 int adamw_plan_create(const adamw_tensor_t* tensors, int32_t n_tensors, int32_t state_kind,
@@ -389,10 +420,7 @@ int adamw_plan_create(const adamw_tensor_t* tensors, int32_t n_tensors, int32_t 
     }
     std::vector<WorkUnit> units;
     std::vector<int32_t> per;
-    build_units(numels.data(), n_tensors, ue, &units, &per);
-    // the last two waves of the queue in pieces of four tiles
-    const int32_t piece = std::min(ue, 4 * cs::tile_elems(state_kind));
-    split_tail(&units, &per, p->sm_count, ue, piece, 2);
+    build_queue(numels.data(), n_tensors, state_kind, ue, p->sm_count, &units, &per);
     p->h_numel = numels;
     if (units.size() >= (size_t(1) << 31) - (size_t(1) << 20)) { delete p; return CS_ERR_LIMIT; }
     for (int32_t i = 0; i < n_tensors; ++i) p->h_descs[i].n_units = per[i];

@@ -292,11 +292,11 @@ int adamw_state_bytes(const int64_t *numels, int32_t n_tensors, int32_t state_ki
                       int64_t *out_bytes);
 
 /*
- * adamw_build_units -- the plan's work-unit table, computed on the host only
- * (no CUDA call), for inspection and tests. Units are (tensor, start, len)
- * with start a multiple of unit_elems, len <= unit_elems, covering each
- * tensor exactly once, ordered longest first; a tensor with numel 0 has one
- * unit of len 0.
+ * adamw_build_units -- the work-unit cut before the queue's tail is re-cut
+ * (see adamw_build_queue), computed on the host only (no CUDA call), for
+ * inspection and tests. Units are (tensor, start, len) with start a multiple
+ * of unit_elems, len <= unit_elems, covering each tensor exactly once,
+ * ordered longest first; a tensor with numel 0 has one unit of len 0.
  *   numels      host [n_tensors];  unit_elems as for adamw_plan_create.
  *   tensor_out, start_out, len_out  host arrays of capacity `cap` (may be NULL
  *               when cap is 0, to query the count).
@@ -307,6 +307,24 @@ int adamw_state_bytes(const int64_t *numels, int32_t n_tensors, int32_t state_ki
 int adamw_build_units(const int64_t *numels, int32_t n_tensors, int32_t unit_elems,
                       int32_t *tensor_out, int64_t *start_out, int32_t *len_out,
                       int64_t cap, int64_t *n_units_out);
+
+/*
+ * adamw_build_queue -- the exact work queue adamw_plan_create builds for a
+ * state kind on a GPU with `ctas` persistent CTAs (its SM count), on the host
+ * only. It is adamw_build_units' cut, after which the units holding the last
+ * two waves' worth of elements (2 * ctas * unit_elems) are re-cut into
+ * pieces of four tiles (12288 elements for fp32/bf16 moments, 16384 for the
+ * 8-bit kinds, never more than unit_elems) and kept longest first, so CTAs
+ * that take units dynamically finish close together. Starts stay multiples
+ * of 256. Arguments and outputs as adamw_build_units, plus state_kind
+ * (CS_STATE_*) and ctas (>= 1).
+ * Errors: CS_ERR_INVALID_ARGUMENT, CS_ERR_UNSUPPORTED (state kind),
+ * CS_ERR_LIMIT (cap too small: nothing but *n_units_out written).
+ */
+int adamw_build_queue(const int64_t *numels, int32_t n_tensors, int32_t state_kind,
+                      int32_t unit_elems, int32_t ctas, int32_t *tensor_out,
+                      int64_t *start_out, int32_t *len_out, int64_t cap,
+                      int64_t *n_units_out);
 
 /*
  * adamw_step_noalloc -- one fused AdamW step that allocates nothing. The pages

@@ -45,7 +45,7 @@ def _header_defines():
 
 def test_exports_every_declared_symbol(cs):
     declared = _header_functions()
-    assert len(declared) == 12, declared
+    assert len(declared) == 13, declared
     assert sorted(cs.EXPORTS) == declared
     L = cs.lib()
     for name in declared:
@@ -195,3 +195,56 @@ def test_selective_fp32_tensor_needs_no_scales(cs):
     assert rc in (0, -5)
     if rc == 0:
         cs.adamw_plan_destroy(cs.Plan(out.value, 1))
+
+
+def _check_cover(numels, t, s, ln):
+    t, s, ln = np.array(t), np.array(s), np.array(ln)
+    for i, n in enumerate(numels):
+        sel = t == i
+        order = np.argsort(s[sel])
+        ss, ll = s[sel][order], ln[sel][order]
+        if n == 0:
+            assert sel.sum() == 1 and ll[0] == 0
+            continue
+        assert ss[0] == 0 and np.all(ss[1:] == ss[:-1] + ll[:-1]) and ss[-1] + ll[-1] == n
+    return t, s, ln
+
+
+@pytest.mark.parametrize("kind,tile", [("f32", 3072), ("bf16", 3072), ("int8", 4096),
+                                       ("dyn8", 4096)])
+@pytest.mark.parametrize("wl", ["lora", "few_large", "many_small", "mixed"])
+def test_plan_queue_recuts_the_last_two_waves(cs, kind, tile, wl):
+    """The plan's queue: every tensor covered once, longest first, starts on
+    256-element blocks; it is the plain cut up to a point, after which every
+    unit is at most four tiles long, and that re-cut region holds the last
+    two waves' worth of elements (at most one unit more)."""
+    if wl == "mixed":
+        numels = [0, 1, 255, 5000, 49152, 49153, 200000, 1 << 20]
+    else:
+        numels = getattr(workloads, wl)().numels
+    ctas, unit = 152, 49152
+    piece = min(unit, 4 * tile)
+    t, s, ln = _check_cover(numels, *cs.adamw_build_queue(numels, kind, ctas))
+    assert np.all(np.diff(ln) <= 0) and np.all(s % 256 == 0)
+    # the queue is the plain cut up to some position p, then re-cut pieces
+    bt, bs, bl = (np.array(x) for x in cs.adamw_build_units(numels))
+    n = min(len(ln), len(bl))
+    diff = np.flatnonzero((t[:n] != bt[:n]) | (s[:n] != bs[:n]) | (ln[:n] != bl[:n]))
+    p = int(diff[0]) if diff.size else n
+    assert np.all(ln[p:] <= piece)
+    region, total, waves = int(ln[p:].sum()), int(ln.sum()), 2 * ctas * unit
+    assert region >= min(total, waves) or np.all(bl[p:] <= piece)
+    assert region <= waves + unit
+    # and the last two waves' worth of elements hold no unit longer than a piece
+    suffix = np.cumsum(ln[::-1])[::-1]
+    assert np.all(ln[suffix <= waves] <= piece)
+
+
+def test_plan_queue_small_plan_is_all_pieces(cs):
+    numels = [3 * 49152 + 7, 100]
+    t, s, ln = _check_cover(numels, *cs.adamw_build_queue(numels, "int8", 152))
+    assert ln.max() <= 4 * 4096
+    with pytest.raises(cs.CompactStateError):
+        cs.adamw_build_queue(numels, "int8", 0)
+    with pytest.raises(KeyError):
+        cs.adamw_build_queue(numels, "f8", 152)
