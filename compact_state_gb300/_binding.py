@@ -125,11 +125,16 @@ def _check(rc: int, where: str) -> None:
 
 
 def _ptr(x) -> Optional[int]:
-    """Device pointer of a torch tensor, an int address, or None."""
+    """Device pointer of a torch tensor, an int address, or None. Tensors must
+    be contiguous CUDA tensors: the kernels address them as flat arrays."""
     if x is None:
         return None
     if isinstance(x, int):
         return x
+    if not x.is_contiguous():
+        raise ValueError("buffers passed to the step must be contiguous")
+    if x.device.type != "cuda":
+        raise ValueError(f"buffers passed to the step must be CUDA tensors, got {x.device}")
     return int(x.data_ptr())
 
 

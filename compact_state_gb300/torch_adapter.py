@@ -1,8 +1,9 @@
 """Torch-side holder of one parameter set's optimizer state.
 
-Allocates zeroed moment buffers (and int8 block scales), the per-tensor int32
-step counters, and the plan, using torch only for device memory; the step
-itself is ``adamw_step`` in the CUDA library.
+Allocates zeroed moment buffers (8-bit codes and their block scales for the
+8-bit kinds, fp32 moments for tensors kept in fp32), optional fp32 master
+weights, the per-tensor int32 step counters, and the plan, using torch only
+for device memory; the step itself is ``adamw_step`` in the CUDA library.
 """
 from __future__ import annotations
 
@@ -103,4 +104,5 @@ class AdamWState:
         adamw_plan_set_grads(self.plan, self.grads, stream)
 
     def state_tensors(self, i: int):
-        return self.m[i], self.v[i], self.m_scale[i], self.v_scale[i]
+        """(m, v, m_scale, v_scale, master) of tensor i (None where absent)."""
+        return self.m[i], self.v[i], self.m_scale[i], self.v_scale[i], self.master[i]

@@ -248,3 +248,11 @@ def test_plan_queue_small_plan_is_all_pieces(cs):
         cs.adamw_build_queue(numels, "int8", 0)
     with pytest.raises(KeyError):
         cs.adamw_build_queue(numels, "f8", 152)
+
+
+def test_descriptors_reject_strided_and_host_tensors(cs):
+    t = torch.zeros(8, 8)
+    with pytest.raises(ValueError, match="contiguous"):
+        cs.tensor_desc(t[:, 0], 0x20000, 0x30000, 0x40000, numel=8, param_dtype="f32")
+    with pytest.raises(ValueError, match="CUDA"):
+        cs.tensor_desc(t.reshape(-1), 0x20000, 0x30000, 0x40000, numel=64, param_dtype="f32")
