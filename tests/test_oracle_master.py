@@ -14,7 +14,9 @@ parameter is that copy rounded to nearest even:
 * a skipped step (found_inf) or a missing gradient leaves master and model
   parameter bit-identical;
 * a planted mistake, updating from the 16-bit value instead of the master,
-  fails the closed form.
+  fails the closed form;
+* without a master, a 16-bit parameter follows the constant-gradient
+  recurrence from its stored value, rounded by torch's casts, step by step.
 """
 import numpy as np
 import pytest
@@ -94,3 +96,30 @@ def test_planted_update_from_the_16bit_value_fails(monkeypatch):
     monkeypatch.setattr(oadamw.TensorState, "weights", lambda self: self.theta)
     with pytest.raises(AssertionError):
         test_sub_ulp_updates_accumulate_in_the_master("bf16", 0.0)
+
+
+@pytest.mark.parametrize("fmt", ["bf16", "f16"])
+@pytest.mark.parametrize("wd", [0.0, 0.1])
+def test_16bit_params_without_master_follow_rounded_recurrence(fmt, wd):
+    """16-bit params without a master: with a constant gradient (m_hat = g,
+    v_hat = g^2 at every t), each step is theta <- cast(theta*(1 - lr*wd) -
+    lr*g/(|g| + eps)) from the stored value, the cast being torch's
+    fp64 -> fp32 -> 16-bit rounding; the oracle's sequence must equal it."""
+    lr, eps = 3e-3, 1e-8
+    rng = np.random.default_rng(4)
+    theta0 = _torch_cast(rng.normal(0, 0.5, 64), fmt)
+    g = _torch_cast(rng.normal(0, 1e-2, 64), fmt)
+    st = new_state(theta0, fmt, "f32")
+    grp = [dict(GROUP, lr=lr, weight_decay=wd, eps=eps)]
+    th = theta0.copy()
+    for t in range(1, 31):
+        oracle_step([st], grp, [g])
+        # float64 recurrence with the constant-gradient moments, then the casts
+        exact = th * (1.0 - lr * wd) - lr * g / (np.abs(g) + eps)
+        th = _torch_cast(exact.astype(np.float32), fmt)
+        # one 16-bit ulp allowed where the float64 value sits on a rounding
+        # boundary between the fp32 and direct roundings
+        ulp = np.abs(th) * (2.0 ** -7 if fmt == "bf16" else 2.0 ** -10)
+        assert np.all(np.abs(st.theta - th) <= ulp), t
+        th = st.theta.copy()                  # continue from the stored value
+    assert not np.array_equal(st.theta, theta0)
