@@ -13,7 +13,7 @@ Workload shapes follow the pages' own scenarios:
 * ``few_large``   -- eight 4096x4096 fp32 matrices ("few large tensors", the
                      ApexW news piece, where the fused path is said to win).
 * ``llama3_8b``   -- the parameter list of an 8B Llama-3-shaped model, bf16
-                     params and grads.
+                     params and grads (``llama3_8b_layer``: one of its layers).
 * ``many_small``  -- 20,000 tensors with log-uniform sizes in [1, 65536] plus 50
                      4096x1024 matrices ("many small tensors", where the ApexW
                      news piece says fused launches lose), three groups, 10% of
@@ -183,6 +183,15 @@ def llama3_8b(layers: int = 32, hidden: int = 4096, kv: int = 1024,
     return Workload(name=f"llama3_8b_L{layers}", tensors=t, groups=groups,
                     param_dtype="bf16", steps=20, seed=0, param_std=0.02,
                     grad_std=1e-3)
+
+
+def llama3_8b_layer(hidden: int = 4096, kv: int = 1024, inter: int = 14336) -> Workload:
+    """One transformer layer of the ``llama3_8b`` list (9 tensors, 218,112,000
+    elements): the same shapes, dtypes and groups, small enough (about 2.6 GB
+    of state with fp32 moments) for detailed profiler captures."""
+    full = llama3_8b(layers=1, hidden=hidden, kv=kv, inter=inter)
+    t = [x for x in full.tensors if x.name.startswith("layer0.")]
+    return dataclasses.replace(full, name="llama3_8b_layer", tensors=t)
 
 
 def many_small(n_small: int = 20000, n_big: int = 50, big_shape=(4096, 1024),
