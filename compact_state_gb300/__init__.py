@@ -6,8 +6,9 @@ declared in ``include/compact_state.h``). This package is its thin binding:
 ``adamw_grad_prologue``, ``adamw_plan_info``, ``adamw_plan_error``,
 ``adamw_plan_set_debug``,
 ``adamw_plan_destroy``, ``adamw_state_bytes``, ``adamw_build_units``,
-``adamw_build_queue``,
-``adamw_step_noalloc`` and ``adamw_strerror`` keep the C names and only
+``adamw_build_queue``, ``adamw_shard_ranges``,
+``adamw_step_noalloc``, ``adamw_noalloc_error``, ``adamw_noalloc_set_debug``
+and ``adamw_strerror`` keep the C names and only
 marshal arguments. ``torch_adapter`` builds descriptors from torch tensors.
 """
 from ._binding import (  # noqa: F401
@@ -17,8 +18,9 @@ from ._binding import (  # noqa: F401
     CS_TENSOR_STATE_F32, DTYPE_CODES, EIGHT_BIT,
     EXPORTS, STATE_CODES, CompactStateError, Plan, adamw_build_queue, adamw_build_units,
     adamw_grad_prologue,
-    adamw_group_t,
+    adamw_group_t, adamw_noalloc_error, adamw_noalloc_set_debug,
     adamw_plan_create, adamw_plan_destroy, adamw_plan_error, adamw_plan_info,
     adamw_plan_info_t, adamw_plan_set_debug,
-    adamw_plan_set_grads, adamw_state_bytes, adamw_step, adamw_step_noalloc, adamw_strerror,
+    adamw_plan_set_grads, adamw_shard_ranges, adamw_state_bytes, adamw_step,
+    adamw_step_noalloc, adamw_strerror,
     adamw_tensor_t, groups_array, lib, pack_present, tensor_desc)

@@ -75,7 +75,8 @@ _LIB = None
 EXPORTS = ("adamw_plan_create", "adamw_step", "adamw_plan_set_grads", "adamw_plan_info",
            "adamw_plan_destroy", "adamw_state_bytes", "adamw_build_units", "adamw_strerror",
            "adamw_plan_error", "adamw_plan_set_debug", "adamw_step_noalloc",
-           "adamw_grad_prologue", "adamw_build_queue")
+           "adamw_grad_prologue", "adamw_build_queue", "adamw_noalloc_error",
+           "adamw_noalloc_set_debug", "adamw_shard_ranges")
 
 
 def lib() -> ctypes.CDLL:
@@ -108,6 +109,11 @@ def lib() -> ctypes.CDLL:
     L.adamw_step_noalloc.argtypes = [ctypes.POINTER(adamw_tensor_t), i32, i32,
                                      ctypes.POINTER(adamw_group_t), i32,
                                      ctypes.POINTER(ctypes.c_uint32), vp, vp, vp, vp]
+    L.adamw_noalloc_error.argtypes = [ctypes.POINTER(ctypes.c_uint32)]
+    L.adamw_shard_ranges.argtypes = [ctypes.POINTER(i64), i32, i32, i32, ctypes.POINTER(i64),
+                                     ctypes.POINTER(i64), ctypes.POINTER(i64),
+                                     ctypes.POINTER(i64)]
+    L.adamw_noalloc_set_debug.argtypes = [ctypes.c_uint64, ctypes.c_uint32]
     L.adamw_grad_prologue.argtypes = [vp, ctypes.POINTER(ctypes.c_uint32), vp, ctypes.c_float,
                                       vp, vp, vp, vp]
     L.adamw_strerror.argtypes = [ctypes.c_int]
@@ -259,6 +265,20 @@ def adamw_step_noalloc(tensors: Sequence[adamw_tensor_t], state_kind, groups,
     _check(rc, "adamw_step_noalloc")
 
 
+def adamw_noalloc_error() -> int:
+    """Read and clear the no-allocation step's error word on the current
+    device (synchronises the device)."""
+    out = ctypes.c_uint32()
+    _check(lib().adamw_noalloc_error(ctypes.byref(out)), "adamw_noalloc_error")
+    return out.value
+
+
+def adamw_noalloc_set_debug(wait_ns: int = 0, flags: int = 0) -> None:
+    """Test hook: bound on every in-kernel wait and debug flags of later
+    no-allocation steps."""
+    _check(lib().adamw_noalloc_set_debug(int(wait_ns), int(flags)), "adamw_noalloc_set_debug")
+
+
 def adamw_grad_prologue(plan: Plan, grad_present=None, inv_scale=None, max_norm: float = 0.0,
                         found_inf_out=None, grad_norm_out=None, scale_out=None,
                         stream=None) -> None:
@@ -340,3 +360,18 @@ def adamw_build_queue(numels: Sequence[int], state_kind, ctas: int, unit_elems: 
     return _unit_table("adamw_build_queue",
                        lambda a, n, t, s, ln, cap, cnt: L.adamw_build_queue(
                            a, n, sk, int(unit_elems), int(ctas), t, s, ln, cap, cnt), numels)
+
+
+def adamw_shard_ranges(numels: Sequence[int], world: int, rank: int):
+    """(lo, hi, offsets, shard_elems) of rank ``rank`` of ``world``: the part
+    [lo[i], hi[i]) of every tensor the rank updates, each tensor's offset in
+    the flat padded buffer, and the elements per shard (host only)."""
+    n = len(numels)
+    arr = (ctypes.c_int64 * max(n, 1))(*[int(x) for x in numels])
+    lo = (ctypes.c_int64 * max(n, 1))()
+    hi = (ctypes.c_int64 * max(n, 1))()
+    off = (ctypes.c_int64 * max(n, 1))()
+    sh = ctypes.c_int64()
+    _check(lib().adamw_shard_ranges(arr, n, int(world), int(rank), lo, hi, off,
+                                    ctypes.byref(sh)), "adamw_shard_ranges")
+    return list(lo[:n]), list(hi[:n]), list(off[:n]), sh.value

@@ -12,7 +12,13 @@
 // The array is shared by every call on a device and keeps the last call's
 // contents: each call rewrites the tables and clears the words that must start
 // at zero before it launches, so calls that overlap on the GPU race with each
-// other and must be ordered by the caller (one stream, or events).
+// other and must be ordered by the caller (one stream, or events). The error
+// word is the exception: it collects the bits of every call until
+// adamw_noalloc_error() reads and clears it.
+//
+// A call copies its tables from host staging arrays that the next call
+// rewrites, so a captured call would replay with another call's tables; a
+// call on a stream that is being captured is refused.
 #include <algorithm>
 #include <cstdint>
 #include <cstring>
@@ -28,7 +34,7 @@ constexpr int kNaMaxUnits = CS_NOALLOC_MAX_UNITS;
 constexpr size_t kNaDescBytes = sizeof(TensorDesc) * kNaMaxTensors;
 constexpr size_t kNaUnitBytes = sizeof(WorkUnit) * kNaMaxUnits;
 constexpr size_t kNaCommitBytes = ((sizeof(uint32_t) * kNaMaxTensors + 255) / 256) * 256;
-constexpr size_t kNaSchedBytes = 256;
+constexpr size_t kNaSchedBytes = 256;   // [0] next unit, [1] CTAs done, [2] error bits
 constexpr size_t kNaScratchBytes = kNaDescBytes + kNaUnitBytes + kNaCommitBytes + kNaSchedBytes;
 static_assert(kNaMaxTensors <= kSmallWords * 32, "fits the small argument class");
 
@@ -43,9 +49,11 @@ struct NaDevice {
   int grid[5][3];           // persistent grid per [state kind][argument class]
 };
 NaDevice g_dev[kNaMaxDevices];
-std::mutex g_mu;                              // guards set-up and the host staging
+std::mutex g_mu;                              // guards set-up, staging and the hook
 TensorDesc g_stage_descs[kNaMaxTensors];      // host staging of this call's tables
 WorkUnit g_stage_units[kNaMaxUnits];
+uint64_t g_wait_ns = kDefaultWaitNs;          // test hook (adamw_noalloc_set_debug)
+uint32_t g_debug = 0;
 
 // Once per device, with that device current: the array's device address and
 // the persistent grid of every kernel variant.
@@ -92,8 +100,8 @@ int launch_args(const TensorDesc* descs, const WorkUnit* units, uint32_t* commit
   a.sched = sched;
   a.commit = commit;
   a.err = sched + 2;
-  a.wait_ns = kDefaultWaitNs;
-  a.debug = 0;
+  a.wait_ns = g_wait_ns;
+  a.debug = g_debug;
   a.n_units = n_units;
   std::memcpy(a.groups, groups, sizeof(adamw_group_t) * n_groups);
   if (present) {
@@ -124,6 +132,13 @@ extern "C" int adamw_step_noalloc(const adamw_tensor_t* tensors, int32_t n_tenso
     const int rc = host::check_group(groups[g]);
     if (rc) return rc;
   }
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  if (cudaStreamIsCapturing(s, &cap) != cudaSuccess) {
+    cudaGetLastError();
+    return CS_ERR_CUDA;
+  }
+  if (cap != cudaStreamCaptureStatusNone) return CS_ERR_INVALID_ARGUMENT;
   std::lock_guard<std::mutex> lock(g_mu);
   // this call's descriptors and work units, in host staging (no allocation)
   int64_t nu = 0;
@@ -166,14 +181,14 @@ extern "C" int adamw_step_noalloc(const adamw_tensor_t* tensors, int32_t n_tenso
   uint32_t* d_commit = reinterpret_cast<uint32_t*>(base + kNaDescBytes + kNaUnitBytes);
   uint32_t* d_sched =
       reinterpret_cast<uint32_t*>(base + kNaDescBytes + kNaUnitBytes + kNaCommitBytes);
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // tables of this call (pageable host source: staged by the runtime before
-  // the copy returns), then zeroed tickets, scheduler and error words
+  // the copy returns), then zeroed tickets and scheduler words; the error
+  // word (sched[2]) keeps its bits for adamw_noalloc_error
   if (cudaMemcpyAsync(d_descs, g_stage_descs, sizeof(TensorDesc) * n_tensors,
                       cudaMemcpyHostToDevice, s) != cudaSuccess ||
       cudaMemcpyAsync(d_units, g_stage_units, sizeof(WorkUnit) * nu, cudaMemcpyHostToDevice,
                       s) != cudaSuccess ||
-      cudaMemsetAsync(d_commit, 0, kNaCommitBytes + kNaSchedBytes, s) != cudaSuccess)
+      cudaMemsetAsync(d_commit, 0, kNaCommitBytes + 2 * sizeof(uint32_t), s) != cudaSuccess)
     return CS_ERR_CUDA;
   const int32_t n_units = static_cast<int32_t>(nu);
   if (n_groups <= kSmallGroups)
@@ -186,4 +201,37 @@ extern "C" int adamw_step_noalloc(const adamw_tensor_t* tensors, int32_t n_tenso
                                             nd->grid[state_kind][kClassMid], groups, n_groups,
                                             grad_present, step, inv_scale, found_inf,
                                             any_master, s);
+}
+
+extern "C" int adamw_noalloc_error(uint32_t* out_flags) {
+  using namespace cs;
+  if (!out_flags) return CS_ERR_INVALID_ARGUMENT;
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return CS_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_mu);
+  NaDevice* nd = nullptr;
+  const int rc = setup_device(dev, &nd);
+  if (rc) return rc;
+  uint32_t* err = reinterpret_cast<uint32_t*>(nd->scratch + kNaDescBytes + kNaUnitBytes +
+                                              kNaCommitBytes) + 2;
+  uint32_t v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess ||
+      cudaMemcpy(&v, err, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return CS_ERR_CUDA;
+  if (v != 0 && (cudaMemset(err, 0, sizeof(v)) != cudaSuccess ||
+                 cudaDeviceSynchronize() != cudaSuccess))
+    return CS_ERR_CUDA;
+  *out_flags = v;
+  return CS_OK;
+}
+
+extern "C" int adamw_noalloc_set_debug(uint64_t wait_ns, uint32_t flags) {
+  using namespace cs;
+  if (wait_ns == 0) wait_ns = kDefaultWaitNs;
+  if (wait_ns > 60ull * 1000000000ull || (flags & ~uint32_t(kDebugSkipFirstTile)))
+    return CS_ERR_INVALID_ARGUMENT;
+  std::lock_guard<std::mutex> lock(g_mu);
+  g_wait_ns = wait_ns;
+  g_debug = flags;
+  return CS_OK;
 }

@@ -227,7 +227,9 @@ int check_group(const adamw_group_t& g) {
   if (!finite_f(g.lr) || !finite_f(g.eps) || !finite_f(g.weight_decay)) return CS_ERR_HYPERPARAM;
   if (!(g.beta1 >= 0.0f && g.beta1 < 1.0f)) return CS_ERR_HYPERPARAM;
   if (!(g.beta2 >= 0.0f && g.beta2 < 1.0f)) return CS_ERR_HYPERPARAM;
-  if (g.eps < 0.0f) return CS_ERR_HYPERPARAM;
+  // eps keeps the denominator sqrt(v_hat) + eps away from zero: a moment that
+  // is zero, or flushed to zero from a subnormal, would otherwise divide 0/0
+  if (!(g.eps > 0.0f)) return CS_ERR_HYPERPARAM;
   return CS_OK;
 }
 
@@ -345,7 +347,7 @@ const char* adamw_strerror(int status) {
     case CS_ERR_LIMIT: return "size limit exceeded (tensors, groups, elements or capacity)";
     case CS_ERR_CUDA: return "CUDA runtime error";
     case CS_ERR_OUT_OF_MEMORY: return "out of memory";
-    case CS_ERR_HYPERPARAM: return "invalid hyper-parameter (beta outside [0,1), negative eps or non-finite value)";
+    case CS_ERR_HYPERPARAM: return "invalid hyper-parameter (beta outside [0,1), eps not positive or non-finite value)";
     case CS_ERR_WRONG_DEVICE: return "current CUDA device is not the plan's device";
     default: return "unknown status";
   }
@@ -382,6 +384,39 @@ int adamw_build_queue(const int64_t* numels, int32_t n_tensors, int32_t state_ki
   if (ctas < 1) return CS_ERR_INVALID_ARGUMENT;
   return write_units(numels, n_tensors, state_kind, unit_elems, ctas, tensor_out, start_out,
                      len_out, cap, n_units_out);
+}
+
+int adamw_shard_ranges(const int64_t* numels, int32_t n_tensors, int32_t world, int32_t rank,
+                       int64_t* lo_out, int64_t* hi_out, int64_t* offset_out,
+                       int64_t* shard_elems_out) {
+  if (n_tensors < 0 || (n_tensors > 0 && (!numels || !lo_out || !hi_out)))
+    return CS_ERR_INVALID_ARGUMENT;
+  if (world < 1 || rank < 0 || rank >= world) return CS_ERR_INVALID_ARGUMENT;
+  const int64_t B = cs::kInt8Block;
+  // flat layout: every tensor padded to whole 256-element blocks, end to end
+  int64_t flat = 0;
+  for (int32_t i = 0; i < n_tensors; ++i) {
+    if (numels[i] < 0) return CS_ERR_INVALID_ARGUMENT;
+    if (numels[i] > (int64_t(1) << 40)) return CS_ERR_LIMIT;
+    flat += (numels[i] + B - 1) / B * B;
+  }
+  // equal shards of whole blocks: world * shard covers the flat buffer
+  const int64_t blocks = flat / B;
+  const int64_t shard = (blocks + world - 1) / world * B;
+  const int64_t r0 = static_cast<int64_t>(rank) * shard, r1 = r0 + shard;
+  int64_t off = 0;
+  for (int32_t i = 0; i < n_tensors; ++i) {
+    const int64_t n = numels[i];
+    int64_t lo = std::min(std::max<int64_t>(r0 - off, 0), n);
+    int64_t hi = std::min(std::max<int64_t>(r1 - off, 0), n);
+    if (hi <= lo) lo = hi = 0;
+    lo_out[i] = lo;
+    hi_out[i] = hi;
+    if (offset_out) offset_out[i] = off;
+    off += (n + B - 1) / B * B;
+  }
+  if (shard_elems_out) *shard_elems_out = shard;
+  return CS_OK;
 }
 
 int adamw_plan_create(const adamw_tensor_t* tensors, int32_t n_tensors, int32_t state_kind,

@@ -102,7 +102,7 @@ typedef struct adamw_group_t {
     float lr;            /* learning rate, finite                            */
     float beta1;         /* in [0, 1)                                        */
     float beta2;         /* in [0, 1)                                        */
-    float eps;           /* finite, >= 0, added outside the square root      */
+    float eps;           /* finite, > 0, added outside the square root      */
     float weight_decay;  /* decoupled decay: theta *= 1 - lr*weight_decay    */
 } adamw_group_t;
 
@@ -327,6 +327,40 @@ int adamw_build_queue(const int64_t *numels, int32_t n_tensors, int32_t state_ki
                       int64_t *n_units_out);
 
 /*
+ * adamw_shard_ranges -- the part of every tensor that rank `rank` of `world`
+ * updates in a ZeRO-style sharded step, computed on the host only (no CUDA
+ * call). "Fused Optimizers and State Precision", section 06: sharding
+ * (ZeRO / FSDP) decides which rank owns which state, the fused optimizer how
+ * the local state is updated, and the two compose. Because the update is
+ * elementwise (and blockwise for the 8-bit kinds), a step over every rank's
+ * part equals the step over the whole list.
+ * Layout: the tensors end to end in one flat buffer, each padded to a whole
+ * number of 256-element blocks (CS_INT8_BLOCK); the flat buffer is cut into
+ * `world` equal shards of shard_elems = ceil(blocks / world) * 256 elements
+ * (the last shards may hold padding only); rank r owns the flat elements
+ * [r * shard_elems, (r + 1) * shard_elems). Tensor i's part is its elements
+ * [lo[i], hi[i]): lo is a multiple of 256 and hi a multiple of 256 or numel,
+ * so no 8-bit scale block is split between ranks; lo == hi == 0 when the rank
+ * owns none of it.
+ *   numels           host [n_tensors], each >= 0.
+ *   world, rank      1 <= world, 0 <= rank < world.
+ *   lo_out, hi_out   host int64 [n_tensors].
+ *   offset_out       host int64 [n_tensors] or NULL: each tensor's first
+ *                    element in the flat buffer (a multiple of 256).
+ *   shard_elems_out  host int64 or NULL: elements per shard; the padded flat
+ *                    buffer holds world * shard_elems.
+ * A rank steps a plan whose tensor i is the slice [lo[i], hi[i]) of every
+ * buffer (param, reduced grad, m, v; scales from block lo[i] / 256), empty
+ * slices included: every rank then keeps the step counts of every tensor
+ * and advances them identically, given the same grad_present mask and the
+ * same (all-reduced) found_inf.
+ * Errors: CS_ERR_INVALID_ARGUMENT, CS_ERR_LIMIT (a tensor above 2^40).
+ */
+int adamw_shard_ranges(const int64_t *numels, int32_t n_tensors, int32_t world, int32_t rank,
+                       int64_t *lo_out, int64_t *hi_out, int64_t *offset_out,
+                       int64_t *shard_elems_out);
+
+/*
  * adamw_step_noalloc -- one fused AdamW step that allocates nothing. The pages
  * have no counterpart to this entry point; it exists for callers that cannot
  * call cudaMalloc: an allocator or memory pool that runs the step from its own
@@ -334,19 +368,26 @@ int adamw_build_queue(const int64_t *numels, int32_t n_tensors, int32_t state_ki
  * hands all device memory to its own pool at start-up.
  *   Arguments as adamw_plan_create's tensors/state_kind plus adamw_step's
  *   groups/grad_present/step/inv_scale/found_inf/stream; every buffer is the
- *   caller's. Work units are CS_NOALLOC_UNIT elements, as in a default plan,
- *   so results equal adamw_step's on the same inputs.
+ *   caller's. Work units are CS_NOALLOC_UNIT elements, cut and ordered like a
+ *   default plan's units but without a plan's re-cut of the queue's tail
+ *   (adamw_build_units gives the cut), so results equal adamw_step's on the
+ *   same inputs; only the balance of the last units across CTAs differs.
  * Scratch: one file-scope device array of fixed size (descriptors, units,
- * tickets, scheduler words; about 1.3 MB), held by every GPU that loads the
- * library until the process exits. Limits: at most CS_NOALLOC_MAX_TENSORS
- * tensors, CS_NOALLOC_MAX_UNITS work units (3.2e9 elements at full units) and
- * CS_SMALL... groups as adamw_step; beyond them it returns CS_ERR_LIMIT
- * without touching the device.
+ * tickets, scheduler and error words; about 1.3 MB), held by every GPU that
+ * loads the library until the process exits. Limits: at most
+ * CS_NOALLOC_MAX_TENSORS tensors, CS_NOALLOC_MAX_UNITS work units (3.2e9
+ * elements at full units) and CS_MAX_GROUPS groups; beyond them it returns
+ * CS_ERR_LIMIT without touching the device.
  * The first call on a device resolves the array's device address there (with
- * that device current); make that first call before any stream capture.
+ * that device current); make that first call before any stream capture. A
+ * call on a stream that is being captured returns CS_ERR_INVALID_ARGUMENT:
+ * each call uploads its tables from host staging that the next call rewrites.
  * Every call shares the array and rewrites it: calls that overlap on the GPU
  * race, so order them (one stream, or events). Calls are serialised on the
  * host. No cudaMalloc, cudaFree or other allocating routine is called.
+ * A bounded wait that runs out inside the kernel (see adamw_plan_error) sets a
+ * bit in the array's error word, which later calls do not clear: read it with
+ * adamw_noalloc_error.
  * Errors: CS_ERR_INVALID_ARGUMENT, CS_ERR_UNSUPPORTED, CS_ERR_MISALIGNED,
  * CS_ERR_HYPERPARAM, CS_ERR_LIMIT, CS_ERR_CUDA.
  */
@@ -358,6 +399,27 @@ int adamw_step_noalloc(const adamw_tensor_t *tensors, int32_t n_tensors, int32_t
                        const uint32_t *grad_present, int32_t *step,
                        const float *inv_scale, const float *found_inf,
                        struct CUstream_st *stream);
+
+/*
+ * adamw_noalloc_error -- read and clear the error word of adamw_step_noalloc
+ * on the current device (host out): the bits of adamw_plan_error, collected
+ * over every no-allocation step since the last read. 0 means they all ran to
+ * completion. A nonzero value means some step gave up part of its work (its
+ * step counts may have advanced for tensors it did not finish); the next call
+ * starts with a clean queue either way. Synchronises the device; allocates
+ * nothing.
+ * Errors: CS_ERR_INVALID_ARGUMENT, CS_ERR_LIMIT (device ordinal >= 64),
+ * CS_ERR_CUDA.
+ */
+int adamw_noalloc_error(uint32_t *out_flags);
+
+/*
+ * adamw_noalloc_set_debug -- test hook for later adamw_step_noalloc calls in
+ * this process: the bound on every wait and the debug flags, with the meaning
+ * of adamw_plan_set_debug. Normal use never calls it.
+ * Errors: CS_ERR_INVALID_ARGUMENT (unknown flag or bound above 60 s).
+ */
+int adamw_noalloc_set_debug(uint64_t wait_ns, uint32_t flags);
 
 /* adamw_strerror -- static string naming a status code (never NULL). */
 const char *adamw_strerror(int status);

@@ -45,7 +45,7 @@ def _header_defines():
 
 def test_exports_every_declared_symbol(cs):
     declared = _header_functions()
-    assert len(declared) == 13, declared
+    assert len(declared) == 16, declared
     assert sorted(cs.EXPORTS) == declared
     L = cs.lib()
     for name in declared:
@@ -256,3 +256,40 @@ def test_descriptors_reject_strided_and_host_tensors(cs):
         cs.tensor_desc(t[:, 0], 0x20000, 0x30000, 0x40000, numel=8, param_dtype="f32")
     with pytest.raises(ValueError, match="CUDA"):
         cs.tensor_desc(t.reshape(-1), 0x20000, 0x30000, 0x40000, numel=64, param_dtype="f32")
+
+
+@pytest.mark.parametrize("bad", [
+    dict(eps=0.0), dict(eps=-1e-8), dict(eps=float("nan")), dict(beta1=1.0),
+    dict(beta2=-0.1), dict(lr=float("inf")), dict(weight_decay=float("nan")),
+])
+def test_step_rejects_bad_hyperparameters_before_any_cuda_call(cs, bad):
+    """Group validation comes first: eps must be positive (it keeps
+    sqrt(v_hat) + eps away from zero), betas in [0, 1), everything finite.
+    The no-allocation entry point checks groups before touching a device, so
+    this runs without a GPU."""
+    g = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.0)
+    g.update(bad)
+    ga = (cs.adamw_group_t * 1)(cs.adamw_group_t(g["lr"], g["beta1"], g["beta2"], g["eps"],
+                                                 g["weight_decay"]))
+    arr = (cs.adamw_tensor_t * 1)(_desc(cs))
+    rc = cs.lib().adamw_step_noalloc(arr, 1, 0, ga, 1, None, 0x1000, None, None, None)
+    assert rc == cs._binding.CS_ERR_HYPERPARAM
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU path")
+def test_tiny_positive_eps_passes_validation(cs):
+    ga = (cs.adamw_group_t * 1)(cs.adamw_group_t(1e-3, 0.9, 0.999, 1e-30, 0.0))
+    arr = (cs.adamw_tensor_t * 1)(_desc(cs))
+    rc = cs.lib().adamw_step_noalloc(arr, 1, 0, ga, 1, None, 0x1000, None, None, None)
+    assert rc == cs._binding.CS_ERR_CUDA      # past validation, then no device here
+
+
+def test_noalloc_readback_without_gpu_reports_cuda_error(cs):
+    if torch.cuda.is_available():
+        pytest.skip("checks the no-GPU path")
+    out = ctypes.c_uint32(7)
+    assert cs.lib().adamw_noalloc_error(None) == -1
+    assert cs.lib().adamw_noalloc_error(ctypes.byref(out)) == -5
+    assert cs.lib().adamw_noalloc_set_debug(0, 2) == -1
+    assert cs.lib().adamw_noalloc_set_debug(61 * 10 ** 9, 0) == -1
+    assert cs.lib().adamw_noalloc_set_debug(0, 0) == 0
