@@ -97,7 +97,8 @@ def lib() -> ctypes.CDLL:
     L.adamw_plan_set_grads.argtypes = [vp, ctypes.POINTER(vp), vp]
     L.adamw_plan_info.argtypes = [vp, ctypes.POINTER(adamw_plan_info_t)]
     L.adamw_plan_destroy.argtypes = [vp]
-    L.adamw_state_bytes.argtypes = [ctypes.POINTER(i64), i32, i32, ctypes.POINTER(i64)]
+    L.adamw_state_bytes.argtypes = [ctypes.POINTER(i64), ctypes.POINTER(i32), i32, i32,
+                                    ctypes.POINTER(i64)]
     L.adamw_build_units.argtypes = [ctypes.POINTER(i64), i32, i32, ctypes.POINTER(i32),
                                     ctypes.POINTER(i64), ctypes.POINTER(i32), i64,
                                     ctypes.POINTER(i64)]
@@ -323,12 +324,19 @@ def adamw_plan_destroy(plan: Plan) -> None:
         _check(lib().adamw_plan_destroy(h), "adamw_plan_destroy")
 
 
-def adamw_state_bytes(numels: Sequence[int], state_kind="f32") -> int:
+def adamw_state_bytes(numels: Sequence[int], state_kind="f32", flags=None,
+                      min_8bit_size: int = 0) -> int:
+    """Optimizer-state bytes of a tensor list. ``flags``: per-tensor
+    adamw_tensor_t.flags values; ``min_8bit_size`` (8-bit kinds) sets
+    CS_TENSOR_STATE_F32 on tensors with fewer elements, as AdamWState does."""
     sk = STATE_CODES[state_kind] if isinstance(state_kind, str) else int(state_kind)
-    arr = (ctypes.c_int64 * max(len(numels), 1))(*[int(n) for n in numels])
+    n = len(numels)
+    arr = (ctypes.c_int64 * max(n, 1))(*[int(x) for x in numels])
+    if flags is None and min_8bit_size and state_kind in EIGHT_BIT:
+        flags = [CS_TENSOR_STATE_F32 if int(x) < min_8bit_size else 0 for x in numels]
+    fa = None if flags is None else (ctypes.c_int32 * max(n, 1))(*[int(f) for f in flags])
     out = ctypes.c_int64()
-    _check(lib().adamw_state_bytes(arr, len(numels), sk, ctypes.byref(out)),
-           "adamw_state_bytes")
+    _check(lib().adamw_state_bytes(arr, fa, n, sk, ctypes.byref(out)), "adamw_state_bytes")
     return out.value
 
 

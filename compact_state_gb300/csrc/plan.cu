@@ -353,17 +353,21 @@ const char* adamw_strerror(int status) {
   }
 }
 
-int adamw_state_bytes(const int64_t* numels, int32_t n_tensors, int32_t state_kind,
-                      int64_t* out_bytes) {
+int adamw_state_bytes(const int64_t* numels, const int32_t* flags, int32_t n_tensors,
+                      int32_t state_kind, int64_t* out_bytes) {
   if (!out_bytes || n_tensors < 0 || (n_tensors > 0 && !numels)) return CS_ERR_INVALID_ARGUMENT;
   const int sb = state_elem_bytes(state_kind);
   if (sb == 0) return CS_ERR_UNSUPPORTED;
   int64_t total = 0;
   for (int32_t i = 0; i < n_tensors; ++i) {
     const int64_t n = numels[i];
-    if (n < 0) return CS_ERR_INVALID_ARGUMENT;
-    total += 2 * sb * n + 4;   // two moments + a 4-byte step counter
-    if (cs::is_8bit(state_kind))
+    const int32_t f = flags ? flags[i] : 0;
+    if (n < 0 || (f & ~CS_TENSOR_STATE_F32)) return CS_ERR_INVALID_ARGUMENT;
+    const bool f32 = (f & CS_TENSOR_STATE_F32) != 0;
+    if (f32 && !cs::is_8bit(state_kind)) return CS_ERR_INVALID_ARGUMENT;
+    // two moments (fp32 for a tensor kept in fp32) + a 4-byte step counter
+    total += 2 * (f32 ? 4 : sb) * n + 4;
+    if (cs::is_8bit(state_kind) && !f32)
       total += 2 * 4 * ((n + cs::kInt8Block - 1) / cs::kInt8Block);
   }
   *out_bytes = total;

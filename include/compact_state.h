@@ -282,14 +282,18 @@ int adamw_plan_destroy(adamw_plan_t *plan);
  * adamw_state_bytes -- bytes of optimizer state for a tensor list, host only:
  * moments (8 / 4 / 2 bytes per element for fp32 / bf16 / the 8-bit kinds),
  * plus for the 8-bit kinds two fp32 scales per 256-element block of each
- * tensor (every tensor counted in the one kind), plus a 4-byte step
- * counter per tensor. Section 05's payload ledger; the ApexW Unsloth benchmark
- * page's 185.501 / 92.751 / 47.101 MB for its LoRA set follow from it.
- *   numels  host array [n_tensors]; out: host int64.
- * Errors: CS_ERR_INVALID_ARGUMENT, CS_ERR_UNSUPPORTED.
+ * tensor, plus a 4-byte step counter per tensor. A tensor whose flags hold
+ * CS_TENSOR_STATE_F32 (8-bit kinds only, as in adamw_plan_create) counts 8
+ * bytes per element and no scales. Section 05's payload ledger; the ApexW
+ * Unsloth benchmark page's 185.501 / 92.751 / 47.101 MB for its LoRA set
+ * follow from it.
+ *   numels  host array [n_tensors]; flags host array [n_tensors] of
+ *           adamw_tensor_t.flags values, or NULL (all 0); out: host int64.
+ * Errors: CS_ERR_INVALID_ARGUMENT (negative size, unknown flag, fp32 flag
+ * outside an 8-bit kind), CS_ERR_UNSUPPORTED.
  */
-int adamw_state_bytes(const int64_t *numels, int32_t n_tensors, int32_t state_kind,
-                      int64_t *out_bytes);
+int adamw_state_bytes(const int64_t *numels, const int32_t *flags, int32_t n_tensors,
+                      int32_t state_kind, int64_t *out_bytes);
 
 /*
  * adamw_build_units -- the work-unit cut before the queue's tail is re-cut

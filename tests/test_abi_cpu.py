@@ -85,8 +85,23 @@ def test_state_bytes_rejects_bad_input(cs):
         cs.adamw_state_bytes([5, -1], "f32")
     with pytest.raises(KeyError):
         cs.adamw_state_bytes([5], "f8")
-    assert cs.lib().adamw_state_bytes(None, 0, 7, ctypes.byref(ctypes.c_int64())) == -2
-    assert cs.lib().adamw_state_bytes(None, 0, 5, ctypes.byref(ctypes.c_int64())) == -2
+    assert cs.lib().adamw_state_bytes(None, None, 0, 7, ctypes.byref(ctypes.c_int64())) == -2
+    assert cs.lib().adamw_state_bytes(None, None, 0, 5, ctypes.byref(ctypes.c_int64())) == -2
+    with pytest.raises(cs.CompactStateError):      # fp32 flag outside an 8-bit kind
+        cs.adamw_state_bytes([5], "bf16", flags=[1])
+    with pytest.raises(cs.CompactStateError):      # unknown flag
+        cs.adamw_state_bytes([5], "int8", flags=[2])
+
+
+@pytest.mark.parametrize("kind", ["int8", "int8uv", "dyn8"])
+@pytest.mark.parametrize("threshold", [0, 1, 4096, 65537, 10 ** 9])
+def test_selective_state_bytes_equal_oracle_ledger(cs, kind, threshold):
+    """With selective fp32 moments the ABI ledger follows the oracle's."""
+    numels = workloads.many_small().numels + [0, 1, 255, 256, 257]
+    got = cs.adamw_state_bytes(numels, kind, min_8bit_size=threshold)
+    assert got == ostate.state_bytes(numels, kind, min_8bit_size=threshold)
+    flags = [1 if n < threshold else 0 for n in numels]
+    assert cs.adamw_state_bytes(numels, kind, flags=flags) == got
 
 
 @pytest.mark.parametrize("unit", [256, 1024, 32768])
