@@ -16,7 +16,7 @@ namespace cs {
 #define CS_WARPS_BF16 12          // compute warps per CTA, bf16 moments
 #endif
 #ifndef CS_WARPS_INT8
-#define CS_WARPS_INT8 16          // compute warps per CTA, int8 moments
+#define CS_WARPS_INT8 8           // compute warps per CTA, 8-bit moments
 #endif
 
 constexpr int kDefaultUnitElems = CS_NOALLOC_UNIT;     // elements per work unit
@@ -44,12 +44,17 @@ constexpr int block_threads(int state_kind) {
   return 32 * (kProducerWarps + consumer_warps(state_kind));
 }
 // Elements per pipeline stage: 3072 for fp32/bf16 moments (one 4-element
-// group per compute thread with fp32 moments, two with bf16), one
-// 256-element block per compute warp for the 8-bit kinds.
+// group per compute thread with fp32 moments, two with bf16), sixteen
+// 256-element blocks for the 8-bit kinds: two per compute warp, whose code
+// is interleaved, so each warp has twice the independent work in flight and
+// pays the per-tile wait and dispatch once per two blocks (measured on
+// 8 x 4096^2 bf16 params: see the kernel notes).
 constexpr int kElementwiseTile = 3072;
+constexpr int kInt8TileBlocks = 16;
 constexpr int tile_elems(int state_kind) {
-  return is_8bit(state_kind) ? consumer_warps(state_kind) * kInt8Block : kElementwiseTile;
+  return is_8bit(state_kind) ? kInt8TileBlocks * kInt8Block : kElementwiseTile;
 }
+static_assert(kInt8TileBlocks == 2 * CS_WARPS_INT8, "two blocks per compute warp");
 // Bytes of one pipeline stage for a state kind (params sized for fp32, the
 // widest param type, since the param type varies per tensor).
 constexpr int stage_bytes(int state_kind) {
