@@ -37,6 +37,11 @@ from oracle.adamw import TensorState, new_state, oracle_step
 
 F32_RTOL = 2e-6
 EIGHT_BIT = ("int8", "int8uv", "dyn8")
+# fp32 values are graded per tensor, relative to |ref| + the tensor's own rms.
+# A tensor with fewer compared positions than this has no reliable scale of
+# its own (one element near a zero crossing has rms ~ 0), so its rms is
+# floored at the rms of all compared positions of the same quantity.
+SMALL_TENSOR = 32
 
 
 # --------------------------------------------------------------------- metrics
@@ -96,8 +101,15 @@ def param16_excess(gpu, ref, fmt: str) -> float:
     return float(np.max(np.abs(gpu[fin] - ref[fin]) / den))
 
 
-def f32_excess(gpu, ref, rtol=F32_RTOL) -> float:
-    """max |gpu-ref| / (rtol*(|ref|+rms(ref))); <= 1 passes."""
+def _rms(x) -> float:
+    x = np.asarray(x, dtype=np.float64)
+    x = x[np.isfinite(x)]
+    return float(np.sqrt(np.mean(x ** 2))) if x.size else 0.0
+
+
+def f32_excess(gpu, ref, rtol=F32_RTOL, rms_floor: float = 0.0) -> float:
+    """max |gpu-ref| / (rtol*(|ref|+rms)); <= 1 passes. rms is the rms of
+    ``ref`` itself, or ``rms_floor`` when that is larger."""
     gpu = np.asarray(gpu, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     if ref.size == 0:
@@ -107,7 +119,7 @@ def f32_excess(gpu, ref, rtol=F32_RTOL) -> float:
         return float("inf")
     if not fin.any():
         return 0.0
-    rms = float(np.sqrt(np.mean(ref[fin] ** 2)))
+    rms = max(float(np.sqrt(np.mean(ref[fin] ** 2))), rms_floor)
     den = rtol * (np.abs(ref[fin]) + rms)
     den = np.where(den == 0, np.finfo(np.float64).tiny, den)
     return float(np.max(np.abs(gpu[fin] - ref[fin]) / den))
@@ -397,8 +409,7 @@ class Harness:
                 th16r.append(o.theta)
             kind = self.kinds[i]
             if kind == "f32":
-                # fp32 bar relative to the rms over every compared position: a
-                # single-element tensor near a zero crossing has no scale of its own
+                # graded per tensor (see SMALL_TENSOR)
                 mv["m"][0].append(m)
                 mv["m"][1].append(o.m)
                 mv["v"][0].append(v)
@@ -414,17 +425,23 @@ class Harness:
                 upd("m_scale_rel", _scale_rel(ms, o.m_scale))
                 upd("v_scale_rel", _scale_rel(vs, o.v_scale))
         if th_all:
-            th, thr = np.concatenate(th_all), np.concatenate(thr_all)
-            upd("theta_excess", f32_excess(th, thr))
-            upd("theta_maxrel", f32_max_rel(th, thr))
+            _grade_f32(upd, "theta", th_all, thr_all)
         if th16:
-            upd("theta16_excess", param16_excess(np.concatenate(th16), np.concatenate(th16r),
-                                                 self.fmt))
+            upd("theta16_excess", max(param16_excess(g, r, self.fmt)
+                                      for g, r in zip(th16, th16r)))
         for k, (g, r) in mv.items():
             if g:
-                g, r = np.concatenate(g), np.concatenate(r)
-                upd(f"{k}_excess", f32_excess(g, r))
-                upd(f"{k}_maxrel", f32_max_rel(g, r))
+                _grade_f32(upd, k, g, r)
+
+
+def _grade_f32(upd, key, gpu_list, ref_list) -> None:
+    """fp32 bar per tensor: each tensor against its own rms, floored at the
+    pooled rms for tensors with fewer than SMALL_TENSOR compared positions."""
+    pooled = _rms(np.concatenate(ref_list)) if ref_list else 0.0
+    for g, r in zip(gpu_list, ref_list):
+        floor = pooled if np.asarray(r).size < SMALL_TENSOR else 0.0
+        upd(f"{key}_excess", f32_excess(g, r, rms_floor=floor))
+        upd(f"{key}_maxrel", f32_max_rel(g, r))
 
 
 def _scale_rel(a, b) -> float:

@@ -45,15 +45,18 @@ def test_worked_example_on_gpu():
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
-def test_tiny_free_run_fp32_state(dtype):
+def test_tiny_free_run_fp32_state(dtype, record_property):
     wl = workloads.tiny(dtype)
     h = Harness(wl, "f32")
     res = h.run()
     if dtype == "f32":
         check_bars(res, "f32", "f32", forced=False)
     else:
-        # 16-bit params drift by rounding in a free run; reported, loosely bounded
-        assert res.free["theta16_excess"] <= 4, res.free
+        # 16-bit params drift by rounding in a free run: reported. m and v do
+        # not depend on theta, and each step's 16-bit rounding can add at most
+        # one ulp of distance, so K steps stay within K ulps.
+        record_property("theta16_drift", res.free["theta16_excess"])
+        assert res.free["theta16_excess"] <= wl.steps, res.free
         assert res.free["m_excess"] <= 1 and res.free["v_excess"] <= 1, res.free
 
 
