@@ -16,7 +16,7 @@ namespace cs {
 #define CS_WARPS_BF16 12          // compute warps per CTA, bf16 moments
 #endif
 #ifndef CS_WARPS_INT8
-#define CS_WARPS_INT8 8           // compute warps per CTA, 8-bit moments
+#define CS_WARPS_INT8 16          // compute warps per CTA, 8-bit moments
 #endif
 
 constexpr int kDefaultUnitElems = CS_NOALLOC_UNIT;     // elements per work unit
@@ -25,12 +25,26 @@ constexpr int kProducerWarps = 2;                      // tile publisher + unit 
 constexpr int kStageBudget = 216 * 1024;               // dynamic shared memory for stages
 constexpr uint64_t kDefaultWaitNs = 2000000000ull;     // 2 s bound on every wait
 
-// The 8-bit state kinds share one kernel shape (one 256-element block per
+// The 8-bit state kinds share one kernel shape (whole 256-element blocks per
 // compute warp, one byte per moment element).
 constexpr bool is_8bit(int state_kind) {
   return state_kind == CS_STATE_INT8 || state_kind == CS_STATE_INT8_UV ||
          state_kind == CS_STATE_DYN8;
 }
+
+// Kernel variants of one state kind, chosen per plan:
+//   kVarPlain     -- every param dtype, no master weights;
+//   kVarExtended  -- also tensors with fp32 master weights or, in an 8-bit
+//                    plan, tensors kept in fp32 moments (extra per-tile cases
+//                    that cost the plain paths up to 5% when always built in);
+//   kVarP16       -- 8-bit kinds only, every param and grad 16-bit and none of
+//                    the extended cases: the stage holds 2-byte params, so a
+//                    stage of the same shared memory holds twice the tile, and
+//                    each compute warp takes two blocks of it with their code
+//                    interleaved (twice the independent work per warp, the
+//                    per-tile wait and dispatch paid once per two blocks).
+enum Variant : int { kVarPlain = 0, kVarExtended = 1, kVarP16 = 2 };
+
 // bf16 moments move the fewest bytes per element of the elementwise kinds,
 // so their tiles come fastest; with 12 warps each thread takes two 4-element
 // groups per tile and the per-tile overhead (wait, metadata, dispatch) is
@@ -43,33 +57,35 @@ constexpr int consumer_warps(int state_kind) {
 constexpr int block_threads(int state_kind) {
   return 32 * (kProducerWarps + consumer_warps(state_kind));
 }
+// 256-element blocks per compute warp per tile (8-bit kinds).
+constexpr int blocks_per_warp(int variant) { return variant == kVarP16 ? 2 : 1; }
 // Elements per pipeline stage: 3072 for fp32/bf16 moments (one 4-element
-// group per compute thread with fp32 moments, two with bf16), sixteen
-// 256-element blocks for the 8-bit kinds: two per compute warp, whose code
-// is interleaved, so each warp has twice the independent work in flight and
-// pays the per-tile wait and dispatch once per two blocks (measured on
-// 8 x 4096^2 bf16 params: see the kernel notes).
+// group per compute thread with fp32 moments, two with bf16); for the 8-bit
+// kinds one 256-element block per compute warp, two with kVarP16.
 constexpr int kElementwiseTile = 3072;
-constexpr int kInt8TileBlocks = 16;
-constexpr int tile_elems(int state_kind) {
-  return is_8bit(state_kind) ? kInt8TileBlocks * kInt8Block : kElementwiseTile;
+constexpr int tile_elems(int state_kind, int variant = kVarPlain) {
+  return is_8bit(state_kind) ? consumer_warps(state_kind) * blocks_per_warp(variant) * kInt8Block
+                             : kElementwiseTile;
 }
-static_assert(kInt8TileBlocks == 2 * CS_WARPS_INT8, "two blocks per compute warp");
-// Bytes of one pipeline stage for a state kind (params sized for fp32, the
-// widest param type, since the param type varies per tensor).
-constexpr int stage_bytes(int state_kind) {
+// Bytes of one pipeline stage: params sized for fp32 (the widest param type,
+// since it varies per tensor), or for 16-bit params in kVarP16.
+constexpr int stage_bytes(int state_kind, int variant = kVarPlain) {
   return state_kind == CS_STATE_F32    ? tile_elems(state_kind) * 16
          : state_kind == CS_STATE_BF16 ? tile_elems(state_kind) * 12
-                                       : tile_elems(state_kind) * 10 +
-                                             2 * (tile_elems(state_kind) / kInt8Block) * 4;
+                                       : tile_elems(state_kind, variant) *
+                                                 (variant == kVarP16 ? 6 : 10) +
+                                             2 * (tile_elems(state_kind, variant) / kInt8Block) * 4;
 }
-constexpr int stages_for(int state_kind) {
-  return kStageBudget / ((stage_bytes(state_kind) + 127) / 128 * 128) > 16
+constexpr int stages_for(int state_kind, int variant = kVarPlain) {
+  return kStageBudget / ((stage_bytes(state_kind, variant) + 127) / 128 * 128) > 16
              ? 16
-             : kStageBudget / ((stage_bytes(state_kind) + 127) / 128 * 128);
+             : kStageBudget / ((stage_bytes(state_kind, variant) + 127) / 128 * 128);
 }
-static_assert(tile_elems(CS_STATE_INT8) % 1024 == 0 && tile_elems(CS_STATE_F32) % 1024 == 0,
+static_assert(tile_elems(CS_STATE_INT8) % 1024 == 0 && tile_elems(CS_STATE_F32) % 1024 == 0 &&
+                  tile_elems(CS_STATE_INT8, kVarP16) % 1024 == 0,
               "tiles hold whole int8 blocks in 16-byte scale groups");
+static_assert(stages_for(CS_STATE_INT8, kVarP16) >= 4 && stages_for(CS_STATE_INT8) >= 5,
+              "stage rings of the 8-bit kinds");
 static_assert(block_threads(CS_STATE_F32) <= 1024 && block_threads(CS_STATE_INT8) <= 1024,
               "threads per CTA");
 static_assert(kElementwiseTile % (4 * 32 * CS_WARPS_ELEMENTWISE) == 0 &&
@@ -165,13 +181,20 @@ TensorDesc make_desc(const adamw_tensor_t& t, int32_t state_kind, uint8_t flags)
 int check_group(const adamw_group_t& g);
 }  // namespace host
 
-// Launch one step. Defined in step_launch.cu. `master`: some tensor of the
-// launch has fp32 master weights or (8-bit plans) fp32 moments; selects the
-// kernel built with those cases.
-cudaError_t launch_step(int state_kind, ArgClass cls, bool master, const void* args,
-                        int grid, cudaStream_t stream);
-// Max resident CTAs per SM of the kernel for (state_kind, cls); also sets the
-// kernel's dynamic shared memory limit.
-cudaError_t step_kernel_occupancy(int state_kind, ArgClass cls, int* blocks_per_sm);
+// The kernel variant a tensor list needs (Variant above): `extended` when
+// some tensor has fp32 master weights or (8-bit kinds) fp32 moments;
+// `all16` when every tensor with elements has 16-bit params.
+constexpr int pick_variant(int state_kind, bool extended, bool all16) {
+  return extended ? kVarExtended : (is_8bit(state_kind) && all16) ? kVarP16 : kVarPlain;
+}
+
+// Launch one step with the kernel of (state_kind, cls, variant). Defined in
+// step_launch.cu.
+cudaError_t launch_step(int state_kind, ArgClass cls, int variant, const void* args, int grid,
+                        cudaStream_t stream);
+// Max resident CTAs per SM of that kernel; also sets its dynamic shared
+// memory limit.
+cudaError_t step_kernel_occupancy(int state_kind, ArgClass cls, int variant,
+                                  int* blocks_per_sm);
 
 }  // namespace cs

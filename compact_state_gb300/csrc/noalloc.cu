@@ -46,7 +46,7 @@ constexpr int kNaMaxDevices = 64;
 struct NaDevice {
   bool ready;
   unsigned char* scratch;   // device address of g_noalloc_scratch on this device
-  int grid[5][3];           // persistent grid per [state kind][argument class]
+  int grid[5][3][3];        // persistent grid per [state kind][variant][argument class]
 };
 NaDevice g_dev[kNaMaxDevices];
 std::mutex g_mu;                              // guards set-up, staging and the hook
@@ -70,13 +70,16 @@ int setup_device(int dev, NaDevice** out) {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return CS_ERR_CUDA;
     for (int sk = 0; sk < 5; ++sk)
-      for (int c = 0; c < 3; ++c) {
-        int per_sm = 0;
-        if (step_kernel_occupancy(sk, static_cast<ArgClass>(c), &per_sm) != cudaSuccess ||
-            per_sm <= 0)
-          return CS_ERR_CUDA;
-        d.grid[sk][c] = per_sm * sms;
-      }
+      for (int var = 0; var < 3; ++var)
+        for (int c = 0; c < 3; ++c) {
+          d.grid[sk][var][c] = 0;
+          if (var == kVarP16 && !is_8bit(sk)) continue;   // not built
+          int per_sm = 0;
+          if (step_kernel_occupancy(sk, static_cast<ArgClass>(c), var, &per_sm) != cudaSuccess ||
+              per_sm <= 0)
+            return CS_ERR_CUDA;
+          d.grid[sk][var][c] = per_sm * sms;
+        }
     d.scratch = static_cast<unsigned char*>(p);
     d.ready = true;
   }
@@ -89,7 +92,7 @@ int launch_args(const TensorDesc* descs, const WorkUnit* units, uint32_t* commit
                 uint32_t* sched, int32_t n_units, int32_t n_tensors, int state_kind,
                 ArgClass cls, int grid, const adamw_group_t* groups, int32_t n_groups,
                 const uint32_t* present, int32_t* step, const float* inv_scale,
-                const float* found_inf, bool master, cudaStream_t stream) {
+                const float* found_inf, int variant, cudaStream_t stream) {
   StepArgs<G, W> a;
   std::memset(&a, 0, sizeof(a));
   a.descs = descs;
@@ -110,7 +113,7 @@ int launch_args(const TensorDesc* descs, const WorkUnit* units, uint32_t* commit
   } else {
     a.all_present = 1;
   }
-  return launch_step(state_kind, cls, master, &a, std::min(grid, n_units), stream) == cudaSuccess
+  return launch_step(state_kind, cls, variant, &a, std::min(grid, n_units), stream) == cudaSuccess
              ? CS_OK
              : CS_ERR_CUDA;
 }
@@ -143,6 +146,7 @@ extern "C" int adamw_step_noalloc(const adamw_tensor_t* tensors, int32_t n_tenso
   // this call's descriptors and work units, in host staging (no allocation)
   int64_t nu = 0;
   bool any_master = false;
+  bool all16 = true;
   for (int32_t i = 0; i < n_tensors; ++i) {
     const adamw_tensor_t& t = tensors[i];
     uint8_t flags = 0;
@@ -155,6 +159,7 @@ extern "C" int adamw_step_noalloc(const adamw_tensor_t* tensors, int32_t n_tenso
     TensorDesc& d = g_stage_descs[i];
     d = host::make_desc(t, state_kind, flags);
     any_master = any_master || t.master != nullptr || (flags & kStateF32) != 0;
+    all16 = all16 && (t.numel == 0 || t.param_dtype != CS_DTYPE_F32);
     d.n_units = static_cast<int32_t>(units);
     for (int64_t k = 0; k < units; ++k) {
       WorkUnit& w = g_stage_units[nu + k];
@@ -191,16 +196,17 @@ extern "C" int adamw_step_noalloc(const adamw_tensor_t* tensors, int32_t n_tenso
       cudaMemsetAsync(d_commit, 0, kNaCommitBytes + 2 * sizeof(uint32_t), s) != cudaSuccess)
     return CS_ERR_CUDA;
   const int32_t n_units = static_cast<int32_t>(nu);
+  const int var = pick_variant(state_kind, any_master, all16);
   if (n_groups <= kSmallGroups)
     return launch_args<kSmallGroups, kSmallWords>(
         d_descs, d_units, d_commit, d_sched, n_units, n_tensors, state_kind, kClassSmall,
-        nd->grid[state_kind][kClassSmall], groups, n_groups, grad_present, step, inv_scale,
-        found_inf, any_master, s);
+        nd->grid[state_kind][var][kClassSmall], groups, n_groups, grad_present, step, inv_scale,
+        found_inf, var, s);
   return launch_args<kMidGroups, kMidWords>(d_descs, d_units, d_commit, d_sched, n_units,
                                             n_tensors, state_kind, kClassMid,
-                                            nd->grid[state_kind][kClassMid], groups, n_groups,
-                                            grad_present, step, inv_scale, found_inf,
-                                            any_master, s);
+                                            nd->grid[state_kind][var][kClassMid], groups,
+                                            n_groups, grad_present, step, inv_scale, found_inf,
+                                            var, s);
 }
 
 extern "C" int adamw_noalloc_error(uint32_t* out_flags) {

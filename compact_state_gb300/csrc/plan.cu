@@ -21,6 +21,8 @@ struct adamw_plan {
   int32_t max_group = 0;
   int32_t sm_count = 0;
   bool any_master = false;         // some tensor has fp32 masters or fp32 moments in an 8-bit plan
+  bool all16 = true;               // every tensor with elements has 16-bit params
+  int variant = 0;                 // kernel variant (cs::Variant)
   int64_t n_units = 0;
   int64_t total_numel = 0;
   int64_t device_bytes = 0;
@@ -263,7 +265,7 @@ int launch_class(adamw_plan* p, cs::ArgClass cls, const adamw_group_t* groups,
     a.all_present = 1;
   }
   const cudaError_t e =
-      cs::launch_step(p->state_kind, cls, p->any_master, &a, p->grid[cls], stream);
+      cs::launch_step(p->state_kind, cls, p->variant, &a, p->grid[cls], stream);
   return e == cudaSuccess ? CS_OK : CS_ERR_CUDA;
 }
 
@@ -449,10 +451,12 @@ int adamw_plan_create(const adamw_tensor_t* tensors, int32_t n_tensors, int32_t 
       if (rc) { delete p; return rc; }
       p->h_descs[i] = make_desc(t, state_kind, vec);
       p->any_master = p->any_master || t.master != nullptr || (vec & cs::kStateF32) != 0;
+      p->all16 = p->all16 && (t.numel == 0 || t.param_dtype != CS_DTYPE_F32);
       numels[i] = t.numel;
       p->total_numel += t.numel;
       p->max_group = std::max(p->max_group, t.group);
     }
+    p->variant = cs::pick_variant(state_kind, p->any_master, p->all16);
     if (cudaGetDevice(&p->device) != cudaSuccess) { delete p; return CS_ERR_CUDA; }
     if (cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
       delete p; return CS_ERR_CUDA;
@@ -467,7 +471,8 @@ int adamw_plan_create(const adamw_tensor_t* tensors, int32_t n_tensors, int32_t 
 
     for (int c = 0; c < 3; ++c) {
       int per_sm = 0;
-      if (cs::step_kernel_occupancy(state_kind, static_cast<cs::ArgClass>(c), &per_sm) != cudaSuccess ||
+      if (cs::step_kernel_occupancy(state_kind, static_cast<cs::ArgClass>(c), p->variant,
+                                    &per_sm) != cudaSuccess ||
           per_sm <= 0) {
         delete p; return CS_ERR_CUDA;
       }

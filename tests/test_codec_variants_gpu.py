@@ -146,3 +146,42 @@ def test_codec_bit_exact_with_zero_betas(kind):
     assert np.array_equal(st.v[0].cpu().numpy().view(np.uint8), qv.view(np.uint8))
     assert np.array_equal(st.m_scale[0].cpu().numpy(), sm)
     assert np.array_equal(st.v_scale[0].cpu().numpy(), sv)
+
+
+@pytest.mark.parametrize("kind", ["int8", "int8uv", "dyn8"])
+def test_mixed_param_dtypes_in_one_8bit_plan(kind):
+    """An 8-bit plan whose params are all 16-bit runs the kernel variant
+    whose stage holds 2-byte params; a plan that also holds an fp32 tensor
+    runs the general one. Both must give the same bits for the same tensors:
+    the 16-bit tensors stepped in a mixed plan equal the same tensors stepped
+    in a plan of their own, over ragged sizes and several steps."""
+    from compact_state_gb300 import adamw_plan_create, tensor_desc
+    from compact_state_gb300.torch_adapter import AdamWState
+    from tests.parity_harness import _bits_equal
+    sizes = [70001, 8192 * 3, 257, 4099, 1]
+    wl16 = workloads.mixed(sizes, param_dtype="bf16", groups=2, steps=4)
+    wl32 = workloads.mixed([30000, 5], param_dtype="f32", groups=2, steps=4)
+    p16a = [workloads.init_param(wl16, i).reshape(-1).cuda() for i in range(len(sizes))]
+    p16b = [x.clone() for x in p16a]
+    p32 = [workloads.init_param(wl32, i).reshape(-1).cuda() for i in range(2)]
+    g16 = [torch.zeros_like(x) for x in p16a]
+    g32 = [torch.zeros_like(x) for x in p32]
+    alone = AdamWState(p16a, g16, kind, [t.group for t in wl16.tensors])
+    mixed = AdamWState(p16b + p32, g16 + g32, kind,
+                       [t.group for t in wl16.tensors] + [t.group for t in wl32.tensors])
+    groups = [dict(lr=g.lr, beta1=g.beta1, beta2=g.beta2, eps=g.eps,
+                   weight_decay=g.weight_decay) for g in wl16.groups]
+    for s in range(1, 5):
+        for i in range(len(sizes)):
+            g16[i].copy_(workloads.grad(wl16, i, s).reshape(-1))
+        for i in range(2):
+            g32[i].copy_(workloads.grad(wl32, i, s).reshape(-1))
+        alone.run(groups)
+        mixed.run(groups)
+    torch.cuda.synchronize()
+    for i in range(len(sizes)):
+        assert _bits_equal(p16a[i], p16b[i]), i
+        assert _bits_equal(alone.m[i], mixed.m[i]) and _bits_equal(alone.v[i], mixed.v[i]), i
+        assert _bits_equal(alone.m_scale[i], mixed.m_scale[i]), i
+        assert _bits_equal(alone.v_scale[i], mixed.v_scale[i]), i
+    assert torch.equal(alone.step[:len(sizes)], mixed.step[:len(sizes)])
