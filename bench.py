@@ -296,21 +296,38 @@ def run_native(args, wl, rank, world, dev):
     hs = stream.cuda_stream
 
     pro = torch.zeros(3, dtype=torch.float32, device=dev)   # found_inf, norm, scale
+    fi_one = torch.ones(1, dtype=torch.float32, device=dev)
+
+    # The workload's own schedule: tensors without a gradient in a step (the
+    # seeded grad-presence mask) and overflowing steps (found_inf = 1) are
+    # timed as configured; a step updates only its present tensors.
+    n_t = len(wl.tensors)
+    schedule = []
+    for s_ in range(1, wl.steps + 1):
+        pres = wl.present(s_)
+        bits = None if pres.all() else cs.pack_present(pres, n_t)
+        upd = int(sum(t.numel for t, p in zip(wl.tensors, pres) if p))
+        schedule.append((bits, bool(wl.found_inf(s_)), upd))
+
+    def sched(k):
+        return schedule[k % len(schedule)]
 
     def one(k):
         plan = plans[k % len(plans)].handle
+        bits, skip, _ = sched(k)
+        fi_k = fi_one if skip else fi
         if args.prologue is not None:
             # unscale, non-finite check and clip first; the step takes their result
-            rc = L.adamw_grad_prologue(plan, None, inv.data_ptr(), float(args.prologue),
+            rc = L.adamw_grad_prologue(plan, bits, inv.data_ptr(), float(args.prologue),
                                        pro.data_ptr(), pro.data_ptr() + 4,
                                        pro.data_ptr() + 8, hs)
             if rc:
                 raise cs.CompactStateError(rc, "adamw_grad_prologue")
-            rc = L.adamw_step(plan, groups, ng, None, st.step.data_ptr(), pro.data_ptr() + 8,
-                              pro.data_ptr(), hs)
+            rc = L.adamw_step(plan, groups, ng, bits, st.step.data_ptr(), pro.data_ptr() + 8,
+                              fi_k.data_ptr() if skip else pro.data_ptr(), hs)
         else:
-            rc = L.adamw_step(plan, groups, ng, None, st.step.data_ptr(), inv.data_ptr(),
-                              fi.data_ptr(), hs)
+            rc = L.adamw_step(plan, groups, ng, bits, st.step.data_ptr(), inv.data_ptr(),
+                              fi_k.data_ptr(), hs)
         if rc:
             raise cs.CompactStateError(rc, "adamw_step")
 
@@ -341,29 +358,47 @@ def run_native(args, wl, rank, world, dev):
     clocks = clk.stop() if rank == 0 else None
     max_ms = allreduce_max(total_ms, world, dev)
     elems = wl.total_numel
-    value = world * elems * K / (max_ms / 1e3)
-    avg_kernel_ms = sum(per) / len(per)
     # per tensor: tensors an 8-bit plan keeps in fp32 move fp32-state bytes
-    bpe = sum(t.numel * bytes_per_elem(wl.param_dtype, "f32" if f32 else state, args.master)
-              for t, f32 in zip(wl.tensors, st.fp32_state)) / max(elems, 1)
-    if args.prologue is not None:
-        bpe += 4 if wl.param_dtype == "f32" else 2     # the prologue reads the grads once more
-    alg_bytes = elems * bpe
+    tbytes = [t.numel * bytes_per_elem(wl.param_dtype, "f32" if f32 else state, args.master)
+              + (t.numel * (4 if wl.param_dtype == "f32" else 2) if args.prologue is not None
+                 else 0)        # the prologue reads the grads once more
+              for t, f32 in zip(wl.tensors, st.fp32_state)]
+    bpe = sum(tbytes) / max(elems, 1)
+    # elements and bytes each timed step updates (its present tensors; none
+    # when the step is skipped for overflow)
+    upd, ubytes, run_ms, skip_ms = [], [], [], []
+    for k in range(K):
+        bits, skip, n_upd = sched(args.warmup + k)
+        if skip:
+            skip_ms.append(per[k])
+            continue
+        pres = wl.present(((args.warmup + k) % len(schedule)) + 1)
+        upd.append(n_upd)
+        ubytes.append(sum(b for b, p in zip(tbytes, pres) if p))
+        run_ms.append(per[k])
+    # value: updated elements of all ranks per second of the timed region
+    value = world * sum(upd) / (max_ms / 1e3)
+    avg_kernel_ms = sum(run_ms) / len(run_ms)
+    alg_bytes = sum(ubytes) / len(ubytes)
     peak, peak_src = hbm_peak()
-    achieved = alg_bytes / (avg_kernel_ms / 1e3) / 1e9
+    achieved = sum(b / (t / 1e3) for b, t in zip(ubytes, run_ms)) / len(run_ms) / 1e9
     key = (args.workload + (f"_{args.param_dtype}" if args.param_dtype else "")
            + ("_master" if args.master else "")
            + (f"_min8bit{args.min_8bit_size}" if args.min_8bit_size else ""))
     traffic = committed_traffic(key, state)
     result = dict(
         value=value, ms_per_step=max_ms / K, kernel_ms_avg=avg_kernel_ms,
-        kernel_ms_median=statistics.median(per), wall_s=wall, clocks=clocks,
+        kernel_ms_median=statistics.median(run_ms), wall_s=wall, clocks=clocks,
         roofline={"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                   "unit": "GB/s", "frac": round(achieved / peak, 4),
                   "traffic": traffic, "peak_source": f"hbm_gbs of {peak_src}",
                   "algorithmic_bytes_per_launch": alg_bytes,
                   "bytes_per_elem": bpe},
-        plan=plan_info, grad_sets=len(plans))
+        plan=plan_info, grad_sets=len(plans),
+        schedule={"elements_updated_per_step": sum(upd) / len(upd),
+                  "steps_skipped_for_overflow": len(skip_ms),
+                  "skipped_step_ms": (sum(skip_ms) / len(skip_ms)) if skip_ms else None,
+                  "grad_none_fraction": wl.none_fraction})
     for p in plans[1:]:
         cs.adamw_plan_destroy(p)
     del sets
@@ -607,7 +642,7 @@ def main(argv=None):
             "e2e": res.get("e2e"), "e2e_offload": res.get("e2e_offload"),
             "gpu_launches": args.steps * (2 if args.prologue is not None else 1),
             "kernel_ms_avg": res["kernel_ms_avg"], "kernel_ms_median": res["kernel_ms_median"],
-            "grad_sets": res["grad_sets"], "cpu_baseline": cb}
+            "grad_sets": res["grad_sets"], "schedule": res["schedule"], "cpu_baseline": cb}
     print(json.dumps(line), flush=True)
     return 0
 
