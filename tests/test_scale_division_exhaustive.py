@@ -19,15 +19,17 @@ float32 division for every positive finite a that matters:
   significands at every field checks that reading as well.
 
 ``--run-slow`` adds the literal sweep over all 2^31 - 2^23 finite positive
-values. Both checks emulate the FMAs exactly: the products below are exact
-in float64, the residual is exact by Sterbenz's lemma (or because both terms
-are multiples of 2^-149 below 2^-100), and the last sum is corrected with its
-exact TwoSum error where float64 rounding lands on an fp32 midpoint.
+values. Both checks emulate the FMAs exactly (tests/fp32_exact.py): products
+are exact in float64, and each fused sum is split exactly by TwoSum and
+rounded to fp32 with its error deciding where float64 lands on an fp32
+midpoint.
 """
 from fractions import Fraction
 
 import numpy as np
 import pytest
+
+from tests.fp32_exact import fma32, mul32
 
 KERNEL_RCP = {127: float.fromhex("0x1.020408p-7"), 255: float.fromhex("0x1.010102p-8")}
 
@@ -47,43 +49,17 @@ def test_reciprocal_constants_are_correctly_rounded():
         assert float(np.float32(c)) == c
 
 
-def _is_f32_midpoint(s: np.ndarray) -> np.ndarray:
-    """float64 values that lie exactly halfway between two fp32 neighbours."""
-    a = np.abs(s)
-    bits = a.view(np.uint64)
-    normal = a >= 2.0 ** -126
-    mid_n = (bits & np.uint64(0x1FFFFFFF)) == np.uint64(0x10000000)
-    k = a * 2.0 ** 150                       # exact: subnormal fp32 midpoints are odd k
-    mid_s = (k == np.floor(k)) & (np.mod(k, 2.0) == 1.0)
-    return np.where(normal, mid_n, mid_s)
-
-
 def emulate(a32: np.ndarray, q: int, q_res: int = None, correct: bool = True) -> np.ndarray:
     """The kernel's three roundings, exactly, for fp32 inputs a32 > 0.
     ``q_res`` and ``correct`` exist only to plant mistakes: the divisor used in
     the residual, and whether the correction step runs at all."""
-    c32 = np.float32(KERNEL_RCP[q])
-    a = a32.astype(np.float64)
-    c = np.float64(c32)
-    q0 = (a * c).astype(np.float32)                  # a*c exact in float64
+    c = np.float32(KERNEL_RCP[q])
+    q0 = mul32(a32, c)
     if not correct:
         return q0
-    qr = q if q_res is None else q_res
-    r = (a - qr * q0.astype(np.float64)).astype(np.float32)   # exact residual, one rounding
-    x = r.astype(np.float64) * c                     # exact in float64
-    y = q0.astype(np.float64)
-    s = x + y                                        # TwoSum: s + err == x + y exactly
-    bb = s - x
-    err = (x - (s - bb)) + (y - bb)
-    out = s.astype(np.float32)                       # nearest even of the float64 sum
-    fix = _is_f32_midpoint(s) & (err != 0.0)
-    if np.any(fix):                                  # the exact sum is off the midpoint
-        up = np.nextafter(out, np.float32(np.inf))
-        dn = np.nextafter(out, np.float32(-np.inf))
-        want_up = err > 0.0
-        out = np.where(fix & want_up & (out.astype(np.float64) < s), up, out)
-        out = np.where(fix & ~want_up & (out.astype(np.float64) > s), dn, out)
-    return out
+    qr = np.float32(q if q_res is None else q_res)
+    r = fma32(-qr, q0, a32)
+    return fma32(r, c, q0)
 
 
 def _check(bits: np.ndarray, q: int, **plant) -> None:
