@@ -185,3 +185,46 @@ def test_mixed_param_dtypes_in_one_8bit_plan(kind):
         assert _bits_equal(alone.m_scale[i], mixed.m_scale[i]), i
         assert _bits_equal(alone.v_scale[i], mixed.v_scale[i]), i
     assert torch.equal(alone.step[:len(sizes)], mixed.step[:len(sizes)])
+
+
+@pytest.mark.parametrize("kind", ["int8", "int8uv", "dyn8"])
+def test_codec_bit_exact_many_scales(kind):
+    """As the test above, with block maxima spread over many decades (the
+    codebook divides by them without an IEEE division per element), with
+    quotients placed at and one ulp beside every codebook midpoint, and with
+    scales that take the IEEE path (below 2^-64, and an all-ones
+    significand): every code and scale equals the oracle's, bit for bit."""
+    from compact_state_gb300.torch_adapter import AdamWState
+    from oracle.adamw import CODECS
+    from oracle import dynamic8
+    rng = np.random.default_rng(99)
+    nblk = 4096
+    s = (rng.uniform(1.0, 2.0, nblk) * 2.0 ** rng.integers(-40, 10, nblk)).astype(np.float32)
+    s[0] = np.float32(2.0 ** -70)                                 # IEEE path: tiny scale
+    s[1] = np.uint32(0x3FFFFFFF).view(np.float32)                 # all-ones significand
+    mids = np.concatenate([dynamic8.SIGNED_MID, dynamic8.UNSIGNED_MID]).astype(np.float32)
+    mids = mids[np.isfinite(mids) & (mids > 0) & (mids < 1)]
+    targets = np.concatenate([mids, np.nextafter(mids, np.float32(0)),
+                              np.nextafter(mids, np.float32(2))])
+    # quotients at and beside the midpoints, and 30% spread over eight decades
+    t = rng.choice(targets, (nblk, 256)).astype(np.float32)
+    spread = rng.random((nblk, 256)) < 0.3
+    t[spread] = (10.0 ** rng.uniform(-8, 0, int(spread.sum()))).astype(np.float32)
+    sign = np.where(rng.random((nblk, 256)) < 0.5, -1.0, 1.0).astype(np.float32)
+    g = (t.astype(np.float64) * s[:, None].astype(np.float64)).astype(np.float32) * sign
+    g[:, 0] = s * sign[:, 0]                                      # the block's max |g| is s
+    g = np.clip(g, -s[:, None], s[:, None]).reshape(-1).astype(np.float32)
+    n = g.size
+    p = torch.zeros(n, dtype=torch.float32, device="cuda")
+    gt = torch.from_numpy(g).cuda()
+    st = AdamWState([p], [gt], kind)
+    st.run([dict(lr=1e-3, beta1=0.0, beta2=0.0, eps=1e-8, weight_decay=0.0)])
+    torch.cuda.synchronize()
+    (enc_m, _, _), (enc_v, _, _) = CODECS[kind]
+    g64 = g.astype(np.float64)
+    qm, sm = enc_m(g64)
+    qv, sv = enc_v((g64 * g64).astype(np.float32).astype(np.float64))
+    assert np.array_equal(st.m_scale[0].cpu().numpy(), sm)
+    assert np.array_equal(st.v_scale[0].cpu().numpy(), sv)
+    assert np.array_equal(st.m[0].cpu().numpy().view(np.uint8), qm.view(np.uint8))
+    assert np.array_equal(st.v[0].cpu().numpy().view(np.uint8), qv.view(np.uint8))
