@@ -203,12 +203,19 @@ void split_tail(std::vector<WorkUnit>* units, std::vector<int32_t>* per_tensor, 
 }
 
 // The queue a plan uses: the unit cut, then the last two waves re-cut into
-// pieces of four tiles.
+// pieces of four tiles; for the 8-bit kinds the last `ctas` of those are cut
+// again into two-tile pieces, which CTAs take one per trip (measured on the
+// LoRA set: 69.5 -> 68.5 us with int8 moments; with bf16 moments the same cut
+// cost 0.7 us, and single-tile pieces were slower for every kind: a one-tile
+// trip is shorter than the fetch that has to hide behind it).
 void build_queue(const int64_t* numels, int32_t n, int32_t state_kind, int32_t unit_elems,
                  int64_t ctas, std::vector<WorkUnit>* units, std::vector<int32_t>* per_tensor) {
   build_units(numels, n, unit_elems, units, per_tensor);
-  const int32_t piece = std::min(unit_elems, 4 * cs::tile_elems(state_kind));
+  const int32_t tile = cs::tile_elems(state_kind);
+  const int32_t piece = std::min(unit_elems, 4 * tile);
   split_tail(units, per_tensor, ctas, unit_elems, piece, 2);
+  if (cs::is_8bit(state_kind) && piece > 2 * tile)
+    split_tail(units, per_tensor, ctas, piece, 2 * tile, 1);
 }
 
 }  // namespace host

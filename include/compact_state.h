@@ -318,10 +318,12 @@ int adamw_build_units(const int64_t *numels, int32_t n_tensors, int32_t unit_ele
  * only. It is adamw_build_units' cut, after which the units holding the last
  * two waves' worth of elements (2 * ctas * unit_elems) are re-cut into
  * pieces of four tiles (12288 elements for fp32/bf16 moments, 16384 for the
- * 8-bit kinds, never more than unit_elems) and kept longest first, so CTAs
- * that take units dynamically finish close together. Starts stay multiples
- * of 256. Arguments and outputs as adamw_build_units, plus state_kind
- * (CS_STATE_*) and ctas (>= 1).
+ * 8-bit kinds, never more than unit_elems); for the 8-bit kinds the units
+ * holding the last ctas such pieces' worth are cut again into two-tile
+ * pieces (8192). All are kept longest first, so CTAs that take units
+ * dynamically finish close together. Starts stay multiples of 256.
+ * Arguments and outputs as adamw_build_units, plus state_kind (CS_STATE_*)
+ * and ctas (>= 1).
  * Errors: CS_ERR_INVALID_ARGUMENT, CS_ERR_UNSUPPORTED (state kind),
  * CS_ERR_LIMIT (cap too small: nothing but *n_units_out written).
  */

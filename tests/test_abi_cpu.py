@@ -250,15 +250,19 @@ def test_plan_queue_recuts_the_last_two_waves(cs, kind, tile, wl):
     region, total, waves = int(ln[p:].sum()), int(ln.sum()), 2 * ctas * unit
     assert region >= min(total, waves) or np.all(bl[p:] <= piece)
     assert region <= waves + unit
-    # and the last two waves' worth of elements hold no unit longer than a piece
+    # the last two waves' worth of elements hold no unit longer than a piece,
+    # and, for the 8-bit kinds, the last ctas pieces' worth none longer than
+    # two tiles
     suffix = np.cumsum(ln[::-1])[::-1]
     assert np.all(ln[suffix <= waves] <= piece)
+    if kind in ("int8", "dyn8"):
+        assert np.all(ln[suffix <= ctas * piece] <= 2 * tile)
 
 
 def test_plan_queue_small_plan_is_all_pieces(cs):
     numels = [3 * 49152 + 7, 100]
     t, s, ln = _check_cover(numels, *cs.adamw_build_queue(numels, "int8", 152))
-    assert ln.max() <= 4 * 4096
+    assert ln.max() <= 2 * 4096
     with pytest.raises(cs.CompactStateError):
         cs.adamw_build_queue(numels, "int8", 0)
     with pytest.raises(KeyError):
