@@ -74,6 +74,7 @@ def load_workload(name: str):
     import workloads
     return {"few_large": workloads.few_large, "llama3_8b": workloads.llama3_8b,
             "llama3_8b_layer": workloads.llama3_8b_layer,
+            "many_small_only": workloads.many_small_only,
             "many_small": workloads.many_small, "lora": workloads.lora,
             "tiny": workloads.tiny}[name]()
 
@@ -556,8 +557,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default="llama3_8b",
-                    choices=["few_large", "llama3_8b", "llama3_8b_layer", "many_small", "lora",
-                             "tiny"])
+                    choices=["few_large", "llama3_8b", "llama3_8b_layer", "many_small",
+                             "many_small_only", "lora", "tiny"])
     ap.add_argument("--state", default="f32", choices=["f32", "bf16", "int8", "int8uv", "dyn8"])
     ap.add_argument("--min-8bit-size", type=int, default=0,
                     help="with an 8-bit state, tensors below this size keep fp32 moments")

@@ -1,8 +1,11 @@
 """Build libcompact_state.so in-tree with nvcc for sm_103a (GB300).
 
-Two translation units are compiled in parallel and linked into one shared
-library with the CUDA runtime linked statically, so the library loads on any
-machine with a CUDA 13 driver. Usage: ``python -m compact_state_gb300.build``.
+The translation units in SOURCES (the host side of the C ABI, the
+no-allocation entry point, the gradient prologue, the launch dispatch, and
+one unit per moment-state kind holding that kind's step kernels) are compiled
+in parallel and linked into one shared library with the CUDA runtime linked
+statically, so the library loads on any machine with a CUDA 13 driver.
+Usage: ``python -m compact_state_gb300.build``.
 """
 from __future__ import annotations
 

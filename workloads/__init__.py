@@ -210,6 +210,15 @@ def many_small(n_small: int = 20000, n_big: int = 50, big_shape=(4096, 1024),
                     found_inf_steps=(5,))
 
 
+def many_small_only(n_small: int = 20000) -> Workload:
+    """The 20,000 log-uniform tensors of ``many_small`` without its 50 large
+    matrices (about 118M elements): the small-tensor part on its own, with
+    the same groups, absent-gradient schedule and overflow step."""
+    full = many_small(n_small=n_small)
+    return dataclasses.replace(full, name=f"many_small_only_{n_small}",
+                               tensors=full.tensors[:n_small])
+
+
 LORA_MODULES = (("q", 3072, 3072), ("k", 3072, 1024), ("v", 3072, 1024),
                 ("o", 3072, 3072), ("gate", 3072, 8192), ("up", 3072, 8192),
                 ("down", 8192, 3072))
