@@ -110,3 +110,53 @@ def test_sharded_fp32_run_matches_the_oracle():
             if hi > lo:
                 assert f32_excess(r.m[i].double().cpu().numpy(), o.m[lo:hi],
                                   rms_floor=float(np.sqrt(np.mean(o.m ** 2)))) <= 1.0
+
+
+def test_sharded_step_through_nccl_on_one_rank():
+    """ShardedAdamW.step() end to end on the GPU: NCCL reduce-scatter of the
+    flat gradients, all-reduce (max) of found_inf, the local fused step and
+    the all-gather of parameters, with one rank (the collectives then move
+    data but exchange nothing). The result must equal the unsharded step bit
+    for bit, including a step whose found_inf is set."""
+    import os
+    import socket
+    import torch.distributed as dist
+    from compact_state_gb300.sharded import ShardedAdamW
+    from compact_state_gb300.torch_adapter import AdamWState
+    if dist.is_initialized():
+        pytest.skip("a process group is already initialised")
+    with socket.socket() as sk:
+        sk.bind(("127.0.0.1", 0))
+        port = sk.getsockname()[1]
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("nccl", rank=0, world_size=1, device_id=torch.device("cuda", 0))
+    try:
+        wl = workloads.mixed(SIZES, param_dtype="bf16", groups=2, steps=4, found_inf_steps=(3,),
+                             grad_prescale=1024.0)
+        grp_of = [t.group for t in wl.tensors]
+        opt = ShardedAdamW(SIZES, "bf16", "int8", grp_of, 1, 0, "cuda")
+        init = [workloads.init_param(wl, i).reshape(-1).cuda() for i in range(len(SIZES))]
+        for i, x in enumerate(init):
+            opt.param(i).copy_(x)
+        ref_p = [x.clone() for x in init]
+        ref_g = [torch.zeros_like(x) for x in init]
+        ref = AdamWState(ref_p, ref_g, "int8", grp_of)
+        groups = [dict(lr=g.lr, beta1=g.beta1, beta2=g.beta2, eps=g.eps,
+                       weight_decay=g.weight_decay) for g in wl.groups]
+        inv = torch.tensor([wl.inv_scale], device="cuda")
+        for s in range(1, 5):
+            fi = torch.tensor([1.0 if wl.found_inf(s) else 0.0], device="cuda")
+            for i in range(len(SIZES)):
+                g = workloads.grad(wl, i, s).reshape(-1).cuda()
+                opt.grad(i).copy_(g)
+                ref_g[i].copy_(g)
+            opt.step(groups, None, inv, fi)
+            ref.run(groups, None, inv, fi)
+        torch.cuda.synchronize()
+        assert torch.equal(opt.step_counts, ref.step)
+        for i in range(len(SIZES)):
+            assert _bits_equal(opt.param(i), ref_p[i]), i
+            if SIZES[i]:
+                assert _bits_equal(opt.m[i], ref.m[i]) and _bits_equal(opt.v[i], ref.v[i]), i
+    finally:
+        dist.destroy_process_group()
