@@ -156,6 +156,11 @@ __device__ __forceinline__ double block_sum(double x) {
 template <int MAXW>
 __global__ void __launch_bounds__(kPrologueThreads, kPrologueBlocksPerSm)
 grad_prologue_kernel(const __grid_constant__ PrologueArgs<MAXW> a) {
+  // Programmatic dependent launch, as in the step kernel: the step launched
+  // next may place its CTAs as this grid's CTAs leave; this grid touches
+  // global memory only once the grids it depends on have completed.
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const float inv = (a.inv_scale != nullptr) ? *a.inv_scale : 1.0f;
   Kahan k;
   bool bad = false;
@@ -257,9 +262,17 @@ cudaError_t occupancy_w(int* blocks_per_sm) {
 
 template <int W>
 cudaError_t launch_w(const void* args, int grid, cudaStream_t stream) {
-  grad_prologue_kernel<W><<<grid, kPrologueThreads, 0, stream>>>(
-      *static_cast<const PrologueArgs<W>*>(args));
-  return cudaGetLastError();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(grid));
+  cfg.blockDim = dim3(kPrologueThreads);
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, grad_prologue_kernel<W>,
+                            *static_cast<const PrologueArgs<W>*>(args));
 }
 
 }  // namespace
