@@ -82,6 +82,24 @@ def test_ragged_multi_unit_free_run_fp32_state(dtype):
         assert res.free["m_excess"] <= 1 and res.free["v_excess"] <= 1, res.free
 
 
+@pytest.mark.parametrize("kind", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", DTYPES)
+def test_packed_small_units(kind, dtype):
+    """Hundreds of small tensors (1 to 1536 elements, most not a multiple of
+    16, so with a direct remainder) share stages several at a time, between
+    larger tensors that take stages of their own; groups, absent gradients and
+    a skipped step as in the ragged cases."""
+    rng = np.random.default_rng(5)
+    sizes = [int(n) for n in rng.integers(1, 1537, 300)]
+    sizes += [1, 15, 16, 17, 1535, 1536, 1537, 3072, 50000, 9]
+    wl = workloads.mixed(sizes, param_dtype=dtype, groups=3, steps=4, none_fraction=0.2,
+                         found_inf_steps=(2,), grad_prescale=1024.0)
+    h = Harness(wl, kind)
+    forced = kind != "f32" or dtype != "f32"
+    res = h.run(forced=forced)
+    check_bars(res, kind, dtype, forced=forced)
+
+
 @pytest.mark.parametrize("kind", KINDS)
 def test_misaligned_buffers_use_scalar_path(kind):
     wl = workloads.mixed([5, 300, 2049], param_dtype="bf16", groups=2, steps=4,
