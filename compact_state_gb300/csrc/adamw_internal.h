@@ -42,8 +42,18 @@ constexpr bool is_8bit(int state_kind) {
 //                    stage of the same shared memory holds twice the tile, and
 //                    each compute warp takes two blocks of it with their code
 //                    interleaved (twice the independent work per warp, the
-//                    per-tile wait and dispatch paid once per two blocks).
-enum Variant : int { kVarPlain = 0, kVarExtended = 1, kVarP16 = 2 };
+//                    per-tile wait and dispatch paid once per two blocks);
+//   kVarP16Pack   -- kVarP16 for lists with small units (kPackMax elements or
+//                    fewer), which it packs several to a stage. A kernel of its
+//                    own: the packing code inside kVarP16 itself cost the
+//                    Llama-3-8B list with int8 moments 0.4-1% of its rate.
+// The plain variant packs small units too (the codebook kind's excepted:
+// its tables leave no shared memory for the segment table).
+enum Variant : int { kVarPlain = 0, kVarExtended = 1, kVarP16 = 2, kVarP16Pack = 3 };
+constexpr int kVariants = 4;
+constexpr bool is_p16(int variant) { return variant == kVarP16 || variant == kVarP16Pack; }
+// Units of at most this many elements are packed (packing kernels only).
+constexpr int kPackMax = 1536;
 
 // bf16 moments move the fewest bytes per element of the elementwise kinds,
 // so their tiles come fastest; with 12 warps each thread takes two 4-element
@@ -58,7 +68,7 @@ constexpr int block_threads(int state_kind) {
   return 32 * (kProducerWarps + consumer_warps(state_kind));
 }
 // 256-element blocks per compute warp per tile (8-bit kinds).
-constexpr int blocks_per_warp(int variant) { return variant == kVarP16 ? 2 : 1; }
+constexpr int blocks_per_warp(int variant) { return is_p16(variant) ? 2 : 1; }
 // Elements per pipeline stage: 3072 for fp32/bf16 moments (one 4-element
 // group per compute thread with fp32 moments, two with bf16); for the 8-bit
 // kinds one 256-element block per compute warp, two with kVarP16.
@@ -73,7 +83,7 @@ constexpr int stage_bytes(int state_kind, int variant = kVarPlain) {
   return state_kind == CS_STATE_F32    ? tile_elems(state_kind) * 16
          : state_kind == CS_STATE_BF16 ? tile_elems(state_kind) * 12
                                        : tile_elems(state_kind, variant) *
-                                                 (variant == kVarP16 ? 6 : 10) +
+                                                 (is_p16(variant) ? 6 : 10) +
                                              2 * (tile_elems(state_kind, variant) / kInt8Block) * 4;
 }
 constexpr int stages_for(int state_kind, int variant = kVarPlain) {
@@ -183,9 +193,12 @@ int check_group(const adamw_group_t& g);
 
 // The kernel variant a tensor list needs (Variant above): `extended` when
 // some tensor has fp32 master weights or (8-bit kinds) fp32 moments;
-// `all16` when every tensor with elements has 16-bit params.
-constexpr int pick_variant(int state_kind, bool extended, bool all16) {
-  return extended ? kVarExtended : (is_8bit(state_kind) && all16) ? kVarP16 : kVarPlain;
+// `all16` when every tensor with elements has 16-bit params; `small` when
+// some work unit has at most kPackMax elements.
+constexpr int pick_variant(int state_kind, bool extended, bool all16, bool small) {
+  return extended                          ? kVarExtended
+         : (is_8bit(state_kind) && all16) ? (small ? kVarP16Pack : kVarP16)
+                                          : kVarPlain;
 }
 
 // Launch one step with the kernel of (state_kind, cls, variant). Defined in

@@ -46,7 +46,7 @@ constexpr int kNaMaxDevices = 64;
 struct NaDevice {
   bool ready;
   unsigned char* scratch;   // device address of g_noalloc_scratch on this device
-  int grid[5][3][3];        // persistent grid per [state kind][variant][argument class]
+  int grid[5][kVariants][3];  // persistent grid per [state kind][variant][argument class]
 };
 NaDevice g_dev[kNaMaxDevices];
 std::mutex g_mu;                              // guards set-up, staging and the hook
@@ -70,10 +70,10 @@ int setup_device(int dev, NaDevice** out) {
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
       return CS_ERR_CUDA;
     for (int sk = 0; sk < 5; ++sk)
-      for (int var = 0; var < 3; ++var)
+      for (int var = 0; var < kVariants; ++var)
         for (int c = 0; c < 3; ++c) {
           d.grid[sk][var][c] = 0;
-          if (var == kVarP16 && !is_8bit(sk)) continue;   // not built
+          if (is_p16(var) && !is_8bit(sk)) continue;   // not built
           int per_sm = 0;
           if (step_kernel_occupancy(sk, static_cast<ArgClass>(c), var, &per_sm) != cudaSuccess ||
               per_sm <= 0)
@@ -196,7 +196,10 @@ extern "C" int adamw_step_noalloc(const adamw_tensor_t* tensors, int32_t n_tenso
       cudaMemsetAsync(d_commit, 0, kNaCommitBytes + 2 * sizeof(uint32_t), s) != cudaSuccess)
     return CS_ERR_CUDA;
   const int32_t n_units = static_cast<int32_t>(nu);
-  const int var = pick_variant(state_kind, any_master, all16);
+  bool small = false;
+  for (int64_t k = 0; k < nu; ++k) small = small || (g_stage_units[k].len > 0 &&
+                                                     g_stage_units[k].len <= kPackMax);
+  const int var = pick_variant(state_kind, any_master, all16, small);
   if (n_groups <= kSmallGroups)
     return launch_args<kSmallGroups, kSmallWords>(
         d_descs, d_units, d_commit, d_sched, n_units, n_tensors, state_kind, kClassSmall,

@@ -463,7 +463,6 @@ int adamw_plan_create(const adamw_tensor_t* tensors, int32_t n_tensors, int32_t 
       p->total_numel += t.numel;
       p->max_group = std::max(p->max_group, t.group);
     }
-    p->variant = cs::pick_variant(state_kind, p->any_master, p->all16);
     if (cudaGetDevice(&p->device) != cudaSuccess) { delete p; return CS_ERR_CUDA; }
     if (cudaDeviceGetAttribute(&p->sm_count, cudaDevAttrMultiProcessorCount, p->device) != cudaSuccess) {
       delete p; return CS_ERR_CUDA;
@@ -471,6 +470,9 @@ int adamw_plan_create(const adamw_tensor_t* tensors, int32_t n_tensors, int32_t 
     std::vector<WorkUnit> units;
     std::vector<int32_t> per;
     build_queue(numels.data(), n_tensors, state_kind, ue, p->sm_count, &units, &per);
+    bool small = false;
+    for (const WorkUnit& w : units) small = small || (w.len > 0 && w.len <= cs::kPackMax);
+    p->variant = cs::pick_variant(state_kind, p->any_master, p->all16, small);
     p->h_numel = numels;
     if (units.size() >= (size_t(1) << 31) - (size_t(1) << 20)) { delete p; return CS_ERR_LIMIT; }
     for (int32_t i = 0; i < n_tensors; ++i) p->h_descs[i].n_units = per[i];

@@ -188,6 +188,40 @@ def test_mixed_param_dtypes_in_one_8bit_plan(kind):
 
 
 @pytest.mark.parametrize("kind", ["int8", "int8uv", "dyn8"])
+def test_16bit_plan_with_small_units_matches_one_without(kind):
+    """A 16-bit-param 8-bit plan whose work units are all large runs the
+    16-bit kernel that never packs; adding small tensors switches the plan to
+    the one that packs them several to a stage. The large tensors must get
+    the same bits from both, over several steps."""
+    from compact_state_gb300.torch_adapter import AdamWState
+    from tests.parity_harness import _bits_equal
+    big, small = [70001, 24576], [300, 7, 1500, 16]
+    wl = workloads.mixed(big + small, param_dtype="bf16", groups=2, steps=3)
+    pa = [workloads.init_param(wl, i).reshape(-1).cuda() for i in range(len(big))]
+    pb = [x.clone() for x in pa]
+    ps = [workloads.init_param(wl, len(big) + i).reshape(-1).cuda() for i in range(len(small))]
+    ga = [torch.zeros_like(x) for x in pa]
+    gs = [torch.zeros_like(x) for x in ps]
+    grp = [t.group for t in wl.tensors]
+    lean = AdamWState(pa, ga, kind, grp[:len(big)])
+    packing = AdamWState(pb + ps, ga + gs, kind, grp)
+    groups = [dict(lr=g.lr, beta1=g.beta1, beta2=g.beta2, eps=g.eps,
+                   weight_decay=g.weight_decay) for g in wl.groups]
+    for s in range(1, 4):
+        for i in range(len(big) + len(small)):
+            (ga + gs)[i].copy_(workloads.grad(wl, i, s).reshape(-1))
+        lean.run(groups)
+        packing.run(groups)
+    torch.cuda.synchronize()
+    for i in range(len(big)):
+        assert _bits_equal(pa[i], pb[i]), i
+        assert _bits_equal(lean.m[i], packing.m[i]) and _bits_equal(lean.v[i], packing.v[i]), i
+        assert _bits_equal(lean.m_scale[i], packing.m_scale[i]), i
+        assert _bits_equal(lean.v_scale[i], packing.v_scale[i]), i
+    assert torch.equal(lean.step[:len(big)], packing.step[:len(big)])
+
+
+@pytest.mark.parametrize("kind", ["int8", "int8uv", "dyn8"])
 def test_codec_bit_exact_many_scales(kind):
     """As the test above, with block maxima spread over many decades (the
     codebook divides by them without an IEEE division per element), with

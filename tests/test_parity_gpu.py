@@ -82,13 +82,14 @@ def test_ragged_multi_unit_free_run_fp32_state(dtype):
         assert res.free["m_excess"] <= 1 and res.free["v_excess"] <= 1, res.free
 
 
-@pytest.mark.parametrize("kind", ["f32", "bf16"])
+@pytest.mark.parametrize("kind", ["f32", "bf16", "int8", "int8uv", "dyn8"])
 @pytest.mark.parametrize("dtype", DTYPES)
 def test_packed_small_units(kind, dtype):
     """Hundreds of small tensors (1 to 1536 elements, most not a multiple of
-    16, so with a direct remainder) share stages several at a time, between
-    larger tensors that take stages of their own; groups, absent gradients and
-    a skipped step as in the ragged cases."""
+    16, so with a direct remainder; for the 8-bit kinds most end in a ragged
+    block) share stages several at a time, between larger tensors that take
+    stages of their own; groups, absent gradients and a skipped step as in the
+    ragged cases. (The codebook kind packs with 16-bit params only.)"""
     rng = np.random.default_rng(5)
     sizes = [int(n) for n in rng.integers(1, 1537, 300)]
     sizes += [1, 15, 16, 17, 1535, 1536, 1537, 3072, 50000, 9]
