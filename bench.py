@@ -29,6 +29,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -61,12 +62,15 @@ KERNEL_SRCS = [os.path.join(ROOT, "compact_state_gb300", "csrc", f)
 
 
 def kernel_hash() -> str:
-    """Hash of the step kernel's sources (a committed traffic figure is only
-    reported while it matches)."""
+    """Hash of the step kernel's code, comments and layout whitespace left
+    out (a committed traffic figure is only reported while it matches)."""
     h = hashlib.sha256()
     for path in KERNEL_SRCS:
-        with open(path, "rb") as f:
-            h.update(f.read())
+        with open(path, encoding="utf-8") as f:
+            src = f.read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()[:16]
 
 
