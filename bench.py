@@ -22,6 +22,11 @@ Prints ONE JSON line (rank 0):
   clocks     SM clocks sampled by nvidia-smi during the timed region
 
 ``--impl reference`` times the CPU oracle instead, on the same metric.
+``--impl torch_fused`` / ``torch_foreach`` time PyTorch's own AdamW
+(``torch.optim.AdamW(fused=True)`` / ``foreach=True``) on the same workload
+and GPU, for context: it keeps its moments in the param dtype, so its line
+compares with this step's ``--state f32`` line for fp32 params and
+``--state bf16`` for 16-bit ones.
 Under torchrun each rank runs an independent replica ("replicas only": the step
 has no exchange); value = elements of all ranks / the slowest rank's time.
 """
@@ -269,6 +274,53 @@ def grad_sets(wl, st, n_sets, dev):
             workloads.fill_grad(wl, i, k + 1, g.view(wl.tensors[i].shape), scratch=scratch)
     del scratch
     return sets
+
+
+def run_torch_adamw(args, wl, dev, impl):
+    """PyTorch's AdamW (``fused=True`` or ``foreach=True``, by ``impl``) over
+    the workload's tensors: one optimizer step
+    per timed step, every gradient present, the workload's groups as param
+    groups. Moments in the param dtype (PyTorch's rule): 28 B/element with
+    fp32 params, 14 with 16-bit ones."""
+    import torch
+    import workloads
+    pdt = workloads.torch_dtype(wl.param_dtype)
+    params = []
+    for i, t in enumerate(wl.tensors):
+        p = torch.empty(t.numel, dtype=pdt, device=dev)
+        p.copy_(workloads.init_param(wl, i, device=dev).reshape(-1))
+        p.grad = torch.empty_like(p)
+        workloads.fill_grad(wl, i, 1, p.grad.view(t.shape))
+        params.append(p)
+    pgroups = [dict(params=[p for p, t in zip(params, wl.tensors) if t.group == k],
+                    lr=g.lr, betas=(g.beta1, g.beta2), eps=g.eps, weight_decay=g.weight_decay)
+               for k, g in enumerate(wl.groups)]
+    mode = {"fused": True} if impl == "torch_fused" else {"foreach": True}
+    opt = torch.optim.AdamW([g for g in pgroups if g["params"]], **mode)
+    for _ in range(args.warmup):
+        opt.step()
+    torch.cuda.synchronize(dev)
+    stream = torch.cuda.current_stream(dev)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    clk = ClockSampler(dev.index if dev.index is not None else 0)
+    clk.start()
+    time.sleep(0.3)
+    clk.mark(True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        opt.step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    clk.mark(False)
+    ms = e0.elapsed_time(e1) / args.steps
+    bpe = 28 if wl.param_dtype == "f32" else 14
+    peak, peak_src = hbm_peak()
+    achieved = wl.total_numel * bpe / (ms / 1e3) / 1e9
+    return {"value": wl.total_numel / (ms / 1e3), "ms_per_step": ms, "clocks": clk.stop(),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": None,
+                         "peak_source": f"hbm_gbs of {peak_src}", "bytes_per_elem": bpe}}
 
 
 def run_native(args, wl, rank, world, dev):
@@ -584,7 +636,8 @@ def main(argv=None):
                     help="with an 8-bit state, tensors below this size keep fp32 moments")
     ap.add_argument("--param-dtype", default=None, choices=["f32", "bf16", "f16"],
                     help="override the workload's param/grad dtype")
-    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--impl", default="native",
+                    choices=["native", "reference", "torch_fused", "torch_foreach"])
     ap.add_argument("--prologue", type=float, default=None, metavar="MAX_NORM",
                     help="run the gradient prologue (non-finite check, norm, clip at "
                          "MAX_NORM) before every step and time both")
@@ -647,6 +700,22 @@ def main(argv=None):
         raise SystemExit("bench.py: no CUDA device (the step has no CPU path)")
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
+    if args.impl in ("torch_fused", "torch_foreach"):
+        if rank != 0:
+            return 0
+        res = run_torch_adamw(args, wl, dev, args.impl)
+        moments = "fp32" if wl.param_dtype == "f32" else wl.param_dtype
+        line = {"impl": args.impl, "metric": metric, "value": res["value"],
+                "unit": "param-elements/s", "n_gpus": 1, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": res["ms_per_step"],
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f32", "data": "synthetic (seeded normal params and grads)",
+                "config": dict(config, state=f"{moments} (PyTorch keeps moments in the "
+                                             f"param dtype)",
+                               grad_none_fraction=0.0, found_inf_steps=[]),
+                "roofline": res["roofline"], "clocks": res["clocks"]}
+        print(json.dumps(line), flush=True)
+        return 0
     from compact_state_gb300 import build
     build.build()
     res = run_native(args, wl, rank, world, dev)

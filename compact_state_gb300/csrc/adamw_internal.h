@@ -44,13 +44,18 @@ constexpr bool is_8bit(int state_kind) {
 //                    interleaved (twice the independent work per warp, the
 //                    per-tile wait and dispatch paid once per two blocks);
 //   kVarP16Pack   -- kVarP16 for lists with small units (kPackMax elements or
-//                    fewer), which it packs several to a stage. A kernel of its
-//                    own: the packing code inside kVarP16 itself cost the
-//                    Llama-3-8B list with int8 moments 0.4-1% of its rate.
-// The plain variant packs small units too (the codebook kind's excepted:
-// its tables leave no shared memory for the segment table).
-enum Variant : int { kVarPlain = 0, kVarExtended = 1, kVarP16 = 2, kVarP16Pack = 3 };
-constexpr int kVariants = 4;
+//                    fewer), which it packs several to a stage;
+//   kVarPlainPack -- kVarPlain for lists with small units, packing them (every
+//                    kind but the codebook one, whose tables leave no shared
+//                    memory for the segment table).
+// The packing kernels are kernels of their own: packing code inside kVarP16
+// cost the Llama-3-8B list with int8 moments 0.4-1% of its rate, inside the
+// bf16-moment kVarPlain 1.5%, through code generation alone (lists without
+// small units never pack).
+enum Variant : int {
+  kVarPlain = 0, kVarExtended = 1, kVarP16 = 2, kVarP16Pack = 3, kVarPlainPack = 4
+};
+constexpr int kVariants = 5;
 constexpr bool is_p16(int variant) { return variant == kVarP16 || variant == kVarP16Pack; }
 // Units of at most this many elements are packed (packing kernels only).
 constexpr int kPackMax = 1536;
@@ -198,7 +203,13 @@ int check_group(const adamw_group_t& g);
 constexpr int pick_variant(int state_kind, bool extended, bool all16, bool small) {
   return extended                          ? kVarExtended
          : (is_8bit(state_kind) && all16) ? (small ? kVarP16Pack : kVarP16)
-                                          : kVarPlain;
+         : (small && state_kind != CS_STATE_DYN8) ? kVarPlainPack
+                                                   : kVarPlain;
+}
+// Whether the kernel of (state_kind, variant) is built.
+constexpr bool variant_built(int state_kind, int variant) {
+  return is_p16(variant) ? is_8bit(state_kind)
+                         : variant != kVarPlainPack || state_kind != CS_STATE_DYN8;
 }
 
 // Launch one step with the kernel of (state_kind, cls, variant). Defined in

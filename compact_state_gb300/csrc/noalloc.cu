@@ -73,7 +73,7 @@ int setup_device(int dev, NaDevice** out) {
       for (int var = 0; var < kVariants; ++var)
         for (int c = 0; c < 3; ++c) {
           d.grid[sk][var][c] = 0;
-          if (is_p16(var) && !is_8bit(sk)) continue;   // not built
+          if (!variant_built(sk, var)) continue;
           int per_sm = 0;
           if (step_kernel_occupancy(sk, static_cast<ArgClass>(c), var, &per_sm) != cudaSuccess ||
               per_sm <= 0)
