@@ -483,6 +483,33 @@ def run_native(args, wl, rank, world, dev):
     return result
 
 
+def link_bandwidth(dev, nbytes=1 << 30, reps=3):
+    """Host-link copy bandwidth of this GPU (GB/s): pinned host -> device,
+    device -> pinned host, and both directions at once on two streams."""
+    import torch
+    n = nbytes // 2
+    h = [torch.empty(n, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    d = [torch.empty(n, dtype=torch.bfloat16, device=dev) for _ in range(2)]
+    s = [torch.cuda.Stream(dev), torch.cuda.Stream(dev)]
+
+    def run(h2d, d2h):
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(reps):
+            if h2d:
+                with torch.cuda.stream(s[0]):
+                    d[0].copy_(h[0], non_blocking=True)
+            if d2h:
+                with torch.cuda.stream(s[1]):
+                    h[1].copy_(d[1], non_blocking=True)
+        torch.cuda.synchronize(dev)
+        return reps * nbytes * (int(h2d) + int(d2h)) / (time.perf_counter() - t0) / 1e9
+
+    run(True, True)   # warm-up
+    return {"h2d": round(run(True, False), 1), "d2h": round(run(False, True), 1),
+            "both": round(run(True, True), 1)}
+
+
 def run_e2e(args, wl, st, groups, ng, dev, world, offload=False):
     """End to end through the public API with host buffers.
 
@@ -585,9 +612,15 @@ def run_e2e(args, wl, st, groups, ng, dev, world, offload=False):
     ms = allreduce_max(e0.elapsed_time(e1), world, dev)
     for p in plans:
         cs.adamw_plan_destroy(p)
+    # the link's own floor for these bytes: each direction alone, and both at once
+    link = link_bandwidth(dev)
+    floor_ms = 1e3 * max(h2d / (link["h2d"] * 1e9), d2h / (link["d2h"] * 1e9),
+                         (h2d + d2h) / (link["both"] * 1e9))
     return {"value": world * wl.total_numel * K / (ms / 1e3), "unit": "param-elements/s",
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": K,
             "ms_per_step": ms / K, "chunks": len(chunks),
+            "link_gbs": link, "link_floor_ms": round(floor_ms, 3),
+            "of_link_floor": round(floor_ms / (ms / K), 4),
             "how": ("params, grads and moments in pinned host memory" if offload else
                     "grads in from pinned host memory, params out; optimizer state "
                     "resident in HBM") +
