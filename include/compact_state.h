@@ -194,7 +194,11 @@ int adamw_plan_create(const adamw_tensor_t *tensors, int32_t n_tensors,
  *                 NULL = 0.
  *   stream        CUDA stream (NULL = legacy default stream).
  * Allocates nothing, does not synchronise, can be captured in a CUDA graph
- * (the group table and bitmask are captured by value).
+ * (the group table and bitmask are captured by value). The kernel is launched
+ * with programmatic dependent launch: it may start on SMs that the previous
+ * kernel on the stream has left (when that kernel allows it, as this step and
+ * adamw_grad_prologue do), but it touches no buffer until the work before it
+ * on the stream has completed and its writes are visible.
  * Errors (nothing is enqueued): CS_ERR_INVALID_ARGUMENT, CS_ERR_HYPERPARAM,
  * CS_ERR_LIMIT, CS_ERR_WRONG_DEVICE; CS_ERR_CUDA if the launch fails.
  */
